@@ -1,0 +1,341 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each pin checks the oracle against what the pages or the mathematics fix:
+hand-worked closed forms (``tests/golden/hand_worked.json``), an independent
+brute-force evaluation on tiny shapes, invariants (softmax rows sum to one,
+uniform V returns V, key permutation invariance), closed forms (Q = 0 gives
+lse = ln|J| and the mean of the attended V rows; one dominant key returns its V
+row), split-KV merge equal to the single pass, and the unmasked case equal to
+``torch.softmax`` in float64.  ``test_pins_catch_planted_mistakes`` plants
+plausible mistakes in a copy of the oracle's C source and checks that the pins
+reject every one.
+"""
+import json
+import math
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from head_attention_forward_fmha_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+HERE = os.path.dirname(os.path.abspath(__file__))
+ORACLE_SRC = os.path.join(os.path.dirname(HERE), "oracle", "fmha_oracle.c")
+
+
+def _arr(spec, n):
+    if spec == "zeros":
+        return np.zeros(n)
+    if spec == "ones":
+        return np.ones(n)
+    return np.asarray(spec, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
+# independent brute force: materialise the score matrix and the mask matrix
+# ----------------------------------------------------------------------------
+def brute_force(q, k, v, scale, window, causal):
+    b, n_h, T, hd = q.shape
+    _, n_kv_h, s_k, _ = k.shape
+    G = n_h // n_kv_h
+    o = np.zeros((b, n_h, T, hd))
+    lse = np.zeros((b, n_h, T))
+    for bi in range(b):
+        for h in range(n_h):
+            kh = h // G
+            S = np.zeros((T, s_k))
+            allowed = np.zeros((T, s_k), dtype=bool)
+            for t in range(T):
+                pos = s_k - T + t
+                for j in range(s_k):
+                    S[t, j] = scale * sum(float(q[bi, h, t, d]) * float(k[bi, kh, j, d]) for d in range(hd))
+                    ok = True
+                    if causal and j > pos:
+                        ok = False
+                    if window > 0 and j <= pos - window:
+                        ok = False
+                    allowed[t, j] = ok
+            for t in range(T):
+                idx = [j for j in range(s_k) if allowed[t, j]]
+                if not idx:
+                    lse[bi, h, t] = -math.inf
+                    continue
+                mx = max(S[t, j] for j in idx)
+                e = {j: math.exp(S[t, j] - mx) for j in idx}
+                tot = sum(e.values())
+                for d in range(hd):
+                    o[bi, h, t, d] = sum(e[j] / tot * float(v[bi, kh, j, d]) for j in idx)
+                lse[bi, h, t] = mx + math.log(tot)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------
+# pins: each raises AssertionError when the oracle disagrees
+# ----------------------------------------------------------------------------
+def pin_golden_cases():
+    data = json.load(open(GOLDEN))
+    for c in data["cases"]:
+        sh = c["shape"]
+        q = _arr(c["q"], sh["batch"] * sh["n_h"] * sh["T"] * sh["hd"]).reshape(
+            sh["batch"], sh["n_h"], sh["T"], sh["hd"])
+        nkv = sh["batch"] * sh["n_kv_h"] * sh["s_k"] * sh["hd"]
+        k = _arr(c["k"], nkv).reshape(sh["batch"], sh["n_kv_h"], sh["s_k"], sh["hd"])
+        v = _arr(c["v"], nkv).reshape(k.shape)
+        o, lse = oracle.attention(q, k, v, c["scale"], c["window"], c["causal"])
+        np.testing.assert_allclose(o.ravel(), c["expect"]["o"], rtol=0, atol=1e-12, err_msg=c["name"])
+        np.testing.assert_allclose(lse.ravel(), c["expect"]["lse"], rtol=0, atol=1e-12, err_msg=c["name"])
+    for c in data["merge_cases"]:
+        op = np.asarray(c["o_parts"], dtype=np.float64).reshape(len(c["o_parts"]), 1, c["hd"])
+        lp = np.asarray([float(x) for x in c["lse_parts"]], dtype=np.float64).reshape(-1, 1)
+        o, lse = oracle.merge(op, lp)
+        np.testing.assert_allclose(o.ravel(), c["expect"]["o"], rtol=0, atol=1e-12, err_msg=c["name"])
+        np.testing.assert_allclose(lse.ravel(), c["expect"]["lse"], rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+TINY = [
+    # batch, n_h, n_kv_h, T, s_k, hd, window, causal
+    (1, 1, 1, 1, 1, 1, 0, False),
+    (1, 2, 1, 3, 5, 2, 0, True),
+    (2, 4, 2, 5, 9, 3, 3, True),
+    (1, 4, 4, 2, 7, 64, 0, False),
+    (2, 2, 1, 4, 6, 2, 2, False),
+    (1, 3, 1, 5, 5, 4, 1, True),
+    (1, 2, 2, 6, 4, 2, 0, False),   # T > s_k, no causal
+]
+
+
+def pin_brute_force_tiny():
+    rng = np.random.default_rng(1)
+    for (b, n_h, n_kv_h, T, s_k, hd, window, causal) in TINY:
+        q = rng.standard_normal((b, n_h, T, hd))
+        k = rng.standard_normal((b, n_kv_h, s_k, hd)) * 2.0
+        v = rng.standard_normal((b, n_kv_h, s_k, hd))
+        scale = 0.7
+        o, lse = oracle.attention(q, k, v, scale, window, causal)
+        ob, lb = brute_force(q, k, v, scale, window, causal)
+        np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isinf(lse), np.isinf(lb))
+        fin = np.isfinite(lb)
+        np.testing.assert_allclose(lse[fin], lb[fin], rtol=0, atol=1e-12)
+
+
+def pin_softmax_rows_sum_to_one():
+    # V = identity over keys: O[t, j] is the softmax weight P[t, j].
+    rng = np.random.default_rng(2)
+    for window, causal in ((0, False), (3, False), (0, True), (4, True)):
+        s_k, hd = 12, 16
+        q = rng.standard_normal((1, 2, 4, hd))
+        k = rng.standard_normal((1, 1, s_k, hd))
+        v = np.zeros((1, 1, s_k, hd))
+        for j in range(s_k):
+            v[0, 0, j, j] = 1.0
+        o, _ = oracle.attention(q, k, v, 0.5, window, causal)
+        assert (o >= 0).all()
+        np.testing.assert_allclose(o.sum(-1), 1.0, rtol=0, atol=1e-12)
+        # masked keys get exactly zero weight
+        for t in range(4):
+            pos = s_k - 4 + t
+            for j in range(s_k):
+                masked = (causal and j > pos) or (window > 0 and j <= pos - window)
+                if masked:
+                    assert (o[0, :, t, j] == 0).all()
+                else:
+                    assert (o[0, :, t, j] > 0).all()
+
+
+def pin_uniform_v_returns_v():
+    rng = np.random.default_rng(3)
+    for (b, n_h, n_kv_h, T, s_k, hd, window, causal) in TINY[1:] + [(2, 8, 2, 3, 40, 8, 7, True)]:
+        q = rng.standard_normal((b, n_h, T, hd)) * 3
+        k = rng.standard_normal((b, n_kv_h, s_k, hd))
+        c = rng.standard_normal(hd)
+        v = np.broadcast_to(c, (b, n_kv_h, s_k, hd)).copy()
+        o, lse = oracle.attention(q, k, v, 1.0, window, causal)
+        np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=0, atol=1e-12)
+
+
+def pin_key_permutation_invariance():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((2, 4, 3, 8))
+    k = rng.standard_normal((2, 2, 17, 8))
+    v = rng.standard_normal((2, 2, 17, 8))
+    perm = rng.permutation(17)
+    o1, l1 = oracle.attention(q, k, v, 0.4)
+    o2, l2 = oracle.attention(q, k[:, :, perm], v[:, :, perm], 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def pin_q_zero_closed_form():
+    # q = 0: every attended score is 0, lse = ln|J| and O = mean of attended V.
+    rng = np.random.default_rng(5)
+    # causal prefill layout: 8 new queries after 24 cached keys
+    T, s_k, hd = 8, 32, 4
+    q = np.zeros((1, 2, T, hd))
+    k = rng.standard_normal((1, 2, s_k, hd))
+    v = rng.standard_normal((1, 2, s_k, hd))
+    o, lse = oracle.attention(q, k, v, 0.3, 0, True)
+    for t in range(T):
+        n = s_k - T + t + 1
+        np.testing.assert_allclose(lse[0, :, t], math.log(n), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o[0, :, t], v[0, :, :n].mean(axis=1), rtol=0, atol=1e-12)
+    # sliding window, decode: lse = ln(window), O = mean of the last `window` rows
+    o, lse = oracle.attention(q[:, :, :1], k, v, 0.3, 5, False)
+    np.testing.assert_allclose(lse, math.log(5), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o[0, :, 0], v[0, :, s_k - 5:].mean(axis=1), rtol=0, atol=1e-12)
+
+
+def pin_dominant_key():
+    rng = np.random.default_rng(6)
+    s_k, hd = 20, 8
+    k = rng.standard_normal((1, 1, s_k, hd)) * 0.01
+    v = rng.standard_normal((1, 1, s_k, hd))
+    jstar = 13
+    q = np.zeros((1, 1, 1, hd))
+    q[0, 0, 0, 0] = 1.0
+    k[0, 0, jstar, 0] = 100.0
+    o, lse = oracle.attention(q, k, v, 1.0)
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, jstar], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0, 0], float(q[0, 0, 0] @ k[0, 0, jstar]), rtol=0, atol=1e-12)
+
+
+def pin_single_attended_key():
+    # window 1: each row attends exactly its own position
+    rng = np.random.default_rng(7)
+    T, s_k, hd = 3, 6, 5
+    q = rng.standard_normal((1, 1, T, hd))
+    k = rng.standard_normal((1, 1, s_k, hd))
+    v = rng.standard_normal((1, 1, s_k, hd))
+    o, lse = oracle.attention(q, k, v, 0.9, 1, True)
+    for t in range(T):
+        j = s_k - T + t
+        np.testing.assert_allclose(o[0, 0, t], v[0, 0, j], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[0, 0, t], 0.9 * float(q[0, 0, t] @ k[0, 0, j]), rtol=0, atol=1e-12)
+
+
+def pin_split_merge_equals_single_pass():
+    rng = np.random.default_rng(8)
+    for (T, s_k, window, causal) in ((1, 600, 0, False), (4, 300, 100, True), (3, 257, 0, True)):
+        q = rng.standard_normal((1, 4, T, 8))
+        k = rng.standard_normal((1, 2, s_k, 8))
+        v = rng.standard_normal((1, 2, s_k, 8))
+        o, lse = oracle.attention(q, k, v, 0.35, window, causal)
+        for chunk in (1, 7, 128, 512, s_k):
+            op, lp = oracle.partials(q, k, v, 0.35, chunk, window, causal)
+            om, lm = oracle.merge(op, lp)
+            np.testing.assert_allclose(om, o, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
+
+
+def pin_split_layout():
+    # chunks start at the first key row 0 attends and cover every attended key
+    assert oracle.split_layout(1, 8192, 4096, 512) == (4096, 8)
+    assert oracle.split_layout(1, 512, 0, 512) == (0, 1)
+    assert oracle.split_layout(128, 512, 0, 100) == (0, 6)
+    assert oracle.split_layout(4, 100, 10, 3) == (87, 5)
+
+
+def pin_torch_softmax_unmasked():
+    # special case that reduces to a library routine: T = 1, no mask
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((2, 6, 1, 16))
+    k = rng.standard_normal((2, 3, 33, 16))
+    v = rng.standard_normal((2, 3, 33, 16))
+    o, lse = oracle.attention(q, k, v, 0.25)
+    tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+    tk = tk.repeat_interleave(2, dim=1)
+    tv = tv.repeat_interleave(2, dim=1)
+    s = (tq @ tk.transpose(-1, -2)) * 0.25
+    np.testing.assert_allclose(o, (torch.softmax(s, -1) @ tv).numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_bf16_widening_is_exact():
+    w = inputs.Workload("t", 1, 2, 1, 2, 40, 64, window=9, causal=True)
+    q, k, v = inputs.make_inputs(w, seed=11)
+    o1, l1 = oracle.attention(inputs.bf16_bits(q), inputs.bf16_bits(k), inputs.bf16_bits(v),
+                              w.scale, w.window, w.causal)
+    o2, l2 = oracle.attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                              w.scale, w.window, w.causal)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def pin_rows_api_matches_full():
+    w = inputs.Workload("t", 2, 4, 2, 3, 50, 16, window=20, causal=True)
+    q, k, v = (inputs.bf16_bits(x) for x in inputs.make_inputs(w, seed=12))
+    o, lse = oracle.attention(q, k, v, w.scale, w.window, w.causal)
+    rows = np.array([0, 5, 7, 23], dtype=np.int64)
+    orow, lrow = oracle.attention_rows(q, k, v, rows, w.scale, w.window, w.causal)
+    np.testing.assert_array_equal(orow, o.reshape(-1, 16)[rows])
+    np.testing.assert_array_equal(lrow, lse.reshape(-1)[rows])
+
+
+ALL_PINS = [pin_golden_cases, pin_brute_force_tiny, pin_softmax_rows_sum_to_one,
+            pin_uniform_v_returns_v, pin_key_permutation_invariance, pin_q_zero_closed_form,
+            pin_dominant_key, pin_single_attended_key, pin_split_merge_equals_single_pass,
+            pin_split_layout, pin_torch_softmax_unmasked, pin_bf16_widening_is_exact,
+            pin_rows_api_matches_full]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
+def test_oracle_pin(pin):
+    pin()
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each mutant of the oracle source must fail at least one pin
+# ----------------------------------------------------------------------------
+MUTANTS = {
+    "dropped_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "gqa_modulo_map": ("int kvh = h / group;", "int kvh = h % n_kv_h;"),
+    "causal_off_by_one": ("if (causal && p < h) h = p;", "if (causal && p - 1 < h) h = p - 1;"),
+    "window_off_by_one": ("l = p - window + 1;", "l = p - window;"),
+    "top_left_alignment": ("long p = (long)s_k - T + t;", "long p = t;"),
+    "lse_missing_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
+    "double_divide": ("double w = exp(s[j] - m) / l;", "double w = exp(s[j] - m) / l / l;"),
+    "v_for_k": ("dot += qd[d] * load_elem(k, kj", "dot += qd[d] * load_elem(v, kj"),
+    "merge_plain_mean": ("double w = exp(lse_parts[(size_t)i * rows + r] - mx) / den;",
+                         "double w = 1.0 / n_splits;"),
+    "merge_lse_log2": ("lse[r] = mx + log(den);", "lse[r] = mx + log2(den);"),
+}
+
+
+def _build_mutant(src_text, tmpdir, name):
+    path = os.path.join(tmpdir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src_text)
+    lib = os.path.join(tmpdir, "lib" + name + ".so")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", lib, "-lm"], check=True)
+    return lib
+
+
+def test_pins_catch_planted_mistakes():
+    src = open(ORACLE_SRC).read()
+    tmpdir = tempfile.mkdtemp(prefix="oracle_mutants_")
+    saved = oracle._lib
+    survivors = []
+    try:
+        for name, (old, new) in MUTANTS.items():
+            assert src.count(old) == 1, "mutation target not found exactly once: " + name
+            lib = _build_mutant(src.replace(old, new), tmpdir, name)
+            oracle._lib = oracle._bind(lib)
+            caught = False
+            for pin in ALL_PINS:
+                try:
+                    pin()
+                except (AssertionError, ValueError):
+                    caught = True
+                    break
+            if not caught:
+                survivors.append(name)
+    finally:
+        oracle._lib = saved
+        shutil.rmtree(tmpdir, ignore_errors=True)
+    assert not survivors, "planted mistakes no pin rejects: %s" % survivors
