@@ -1,0 +1,184 @@
+"""Thin ctypes binding of ``libfmha_gb300.so`` (C ABI in ``include/fmha.h``).
+
+Argument marshalling only: torch tensors are checked for dtype, shape,
+contiguity and device, then their data pointers go to the C entry point of the
+same name.  Every step of the attention forward runs in the library's CUDA
+kernels; there is no CPU fallback, and a missing library raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfmha_gb300.so")
+
+FMHA_OK = 0
+ERRORS = {
+    -1: "FMHA_ERR_NULL", -2: "FMHA_ERR_ALIGN", -3: "FMHA_ERR_HEADDIM", -4: "FMHA_ERR_HEADS",
+    -5: "FMHA_ERR_SHAPE", -6: "FMHA_ERR_WORKSPACE", -7: "FMHA_ERR_LAUNCH", -8: "FMHA_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol include/fmha.h declares, with its ctypes signature.
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fmha_fwd": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
+    "fmha_fwd_plan": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
+    "fmha_split_layout": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
+    "fmha_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp],
+                         _i32),
+    "fmha_merge": ([_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "fmha_splitkv_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32], _sz),
+    "fmha_check_device_status": ([_vp], _i32),
+    "fmha_get_last_error": ([], ctypes.c_char_p),
+    "fmha_release": ([], None),
+    "fmha_version": ([], _i32),
+}
+
+_lib = None
+
+
+class FmhaError(RuntimeError):
+    def __init__(self, code, fn, msg):
+        super().__init__("%s returned %s (%d): %s" % (fn, ERRORS.get(code, "?"), code, msg))
+        self.code = code
+
+
+def load(path=None):
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError("libfmha_gb300.so not found at %s: run head_attention_forward_fmha_gb300.build" % p)
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc, fn):
+    if rc != FMHA_OK:
+        raise FmhaError(rc, fn, load().fmha_get_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _bf16(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA bf16 tensor" % name)
+    return t.data_ptr()
+
+
+def _f32(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA float32 tensor" % name)
+    return t.data_ptr()
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or tuple(k.shape) != tuple(v.shape):
+        raise ValueError("q [b,n_h,T,hd] and k, v [b,n_kv_h,s_k,hd] expected")
+    b, n_h, T, hd = q.shape
+    bk, n_kv_h, s_k, hdk = k.shape
+    if bk != b or hdk != hd:
+        raise ValueError("q %s and k %s disagree" % (tuple(q.shape), tuple(k.shape)))
+    return b, n_h, n_kv_h, T, s_k, hd
+
+
+def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stream=None):
+    """O (bf16 [b,n_h,T,hd]) and LSE (fp32 [b,n_h,T]); allocates them if not given."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, n_h, T), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                         b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)), _stream(stream))
+    _check(rc, "fmha_fwd")
+    return o, lse
+
+
+def fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, window=0, causal=False):
+    """(n_splits, kv_chunk) that fmha_fwd uses for this shape."""
+    chunk = ctypes.c_int(0)
+    n = load().fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, int(window), int(bool(causal)), ctypes.byref(chunk))
+    _check(n if n < 0 else 0, "fmha_fwd_plan")
+    return n, chunk.value
+
+
+def fmha_split_layout(T, s_k, window, kv_chunk):
+    """(first key of chunk 0, number of chunks)."""
+    first = ctypes.c_int(0)
+    n = load().fmha_split_layout(int(T), int(s_k), int(window), int(kv_chunk), ctypes.byref(first))
+    _check(n if n < 0 else 0, "fmha_split_layout")
+    return first.value, n
+
+
+def fmha_fwd_splitkv(q, k, v, kv_chunk, o_parts=None, lse_parts=None, scale=None, window=0, causal=False,
+                     stream=None):
+    """fp32 partials O_i [n,b,n_h,T,hd] and lse_i [n,b,n_h,T] for chunks of kv_chunk keys."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    _, n = fmha_split_layout(T, s_k, window, kv_chunk)
+    if o_parts is None:
+        o_parts = torch.empty((n, b, n_h, T, hd), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((n, b, n_h, T), dtype=torch.float32, device=q.device)
+    if o_parts.numel() < n * b * n_h * T * hd or lse_parts.numel() < n * b * n_h * T:
+        raise ValueError("partial buffers too small for %d chunks" % n)
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd_splitkv(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _f32(o_parts, "o_parts"),
+                                 _f32(lse_parts, "lse_parts"), int(kv_chunk), b, n_h, n_kv_h, T, s_k, hd,
+                                 float(scale), int(window), int(bool(causal)), _stream(stream))
+    _check(rc, "fmha_fwd_splitkv")
+    return o_parts, lse_parts
+
+
+def fmha_merge(o_parts, lse_parts, o=None, lse=None, stream=None):
+    """Merge partials [n,b,n_h,T,hd] / [n,b,n_h,T] into bf16 O and fp32 LSE."""
+    if o_parts.dim() != 5 or lse_parts.dim() != 4 or tuple(o_parts.shape[:4]) != tuple(lse_parts.shape):
+        raise ValueError("o_parts [n,b,n_h,T,hd] and lse_parts [n,b,n_h,T] expected")
+    n, b, n_h, T, hd = o_parts.shape
+    if o is None:
+        o = torch.empty((b, n_h, T, hd), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((b, n_h, T), dtype=torch.float32, device=o_parts.device)
+    rc = load().fmha_merge(_f32(o_parts, "o_parts"), _f32(lse_parts, "lse_parts"), n, _bf16(o, "o"),
+                           _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
+    _check(rc, "fmha_merge")
+    return o, lse
+
+
+def fmha_splitkv_workspace_bytes(batch, n_h, T, hd, n_splits):
+    return int(load().fmha_splitkv_workspace_bytes(batch, n_h, T, hd, n_splits))
+
+
+def fmha_check_device_status(stream=None):
+    rc = load().fmha_check_device_status(_stream(stream))
+    _check(rc, "fmha_check_device_status")
+
+
+def fmha_get_last_error():
+    return load().fmha_get_last_error().decode(errors="replace")
+
+
+def fmha_release():
+    load().fmha_release()
+
+
+def fmha_version():
+    return int(load().fmha_version())

@@ -1,0 +1,353 @@
+// api.cu -- the C ABI of libfmha_gb300.so (declared in include/fmha.h).
+//
+// Validates arguments, plans the split-KV layout, builds the TMA tensor maps
+// for K and V, and launches the kernels on the caller's stream.  No call here
+// synchronises the host except fmha_check_device_status() and fmha_release().
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "fmha.h"
+#include "internal.h"
+
+namespace {
+
+using namespace fmha;
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(FMHA_ERR_LAUNCH, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool tensor_map_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// K or V [slabs, s_k, hd] bf16 viewed as a 3-D tensor (hd fastest); boxes of
+// 64 head-dim columns (128 bytes, 128-byte swizzle) x box_rows keys x 1 slab.
+int make_kv_map(CUtensorMap* m, const void* base, int hd, int s_k, long long slabs, int box_rows) {
+    std::memset(m, 0, sizeof *m);
+    if (s_k == 0) return FMHA_OK;  // nothing will be loaded
+    if (!tensor_map_encoder()) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)s_k, (cuuint64_t)slabs};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)s_k * hd * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return FMHA_OK;
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                Problem* out) {
+    if (hd != 64 && hd != 128 && hd != 256 && hd != 512)
+        return fail(FMHA_ERR_HEADDIM, "hd=%d: supported head dims are 64, 128, 256, 512", hd);
+    if (n_h < 1 || n_kv_h < 1 || n_h % n_kv_h != 0)
+        return fail(FMHA_ERR_HEADS, "n_h=%d n_kv_h=%d: need n_h, n_kv_h >= 1 and n_h %% n_kv_h == 0", n_h, n_kv_h);
+    if (batch < 0 || T < 0 || s_k < 0)
+        return fail(FMHA_ERR_SHAPE, "negative size (batch=%d T=%d s_k=%d)", batch, T, s_k);
+    if (causal != 0 && causal != 1) return fail(FMHA_ERR_SHAPE, "causal must be 0 or 1 (got %d)", causal);
+    if (causal && T > s_k)
+        return fail(FMHA_ERR_SHAPE, "causal with T=%d > s_k=%d leaves query rows with no key", T, s_k);
+    if (window < 0) return fail(FMHA_ERR_SHAPE, "window=%d must be >= 0", window);
+    if (!std::isfinite(scale)) return fail(FMHA_ERR_SHAPE, "scale must be finite");
+    if ((long long)batch * n_kv_h > 65535)
+        return fail(FMHA_ERR_SHAPE, "batch * n_kv_h = %lld exceeds 65535", (long long)batch * n_kv_h);
+    if ((long long)n_h / n_kv_h * T > (1LL << 30)) return fail(FMHA_ERR_SHAPE, "too many query rows per KV head");
+    out->batch = batch;
+    out->n_h = n_h;
+    out->n_kv_h = n_kv_h;
+    out->T = T;
+    out->s_k = s_k;
+    out->hd = hd;
+    out->window = window;
+    out->causal = causal;
+    out->scale = scale;
+    out->group = n_h / n_kv_h;
+    out->R = out->group * T;
+    return FMHA_OK;
+}
+
+// k and v may be NULL only when there is no key (s_k == 0).
+int check_inputs(const void* q, const void* k, const void* v, int s_k) {
+    if (!q || ((!k || !v) && s_k > 0)) return fail(FMHA_ERR_NULL, "q, k and v must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return fail(FMHA_ERR_ALIGN, "q, k and v must be 16-byte aligned");
+    return FMHA_OK;
+}
+
+// First attended key of row t = 0 and the chunk count for chunks of `chunk`.
+SplitPlan split_layout(int T, int s_k, int window, int chunk) {
+    long long first = 0;
+    if (window > 0) {
+        const long long p = (long long)s_k - T;  // position of row 0
+        first = p - window + 1;
+        if (first < 0) first = 0;
+    }
+    SplitPlan sp;
+    sp.kv_begin = (int)first;
+    sp.kv_chunk = chunk;
+    const long long span = (long long)s_k - first;
+    sp.n_splits = (span <= 0) ? 1 : (int)((span + chunk - 1) / chunk);
+    return sp;
+}
+
+int sm_count() {
+    static int cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Split heuristic: enough thread blocks to fill every SM a few times over,
+// but chunks of at least 256 keys.
+SplitPlan choose_split(const Problem& p) {
+    const int kt = decode_kv_tile(p.hd);
+    const int rows = decode_rows_per_cta(p.hd, p.R);
+    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + rows - 1) / rows);
+    SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
+    const long long span = (long long)p.s_k - whole.kv_begin;
+    const int per_sm = (p.hd == 512) ? 1 : 2;
+    const long long target = 4LL * sm_count() * per_sm;
+    if (units <= 0 || span <= 256 || units >= target) return whole;
+    long long n = (target + units - 1) / units;
+    const long long max_n = span / 256;
+    if (n > max_n) n = max_n;
+    if (n <= 1) return whole;
+    long long chunk = (span + n - 1) / n;
+    chunk = (chunk + kt - 1) / kt * kt;
+    return split_layout(p.T, p.s_k, p.window, (int)chunk);
+}
+
+// ---------------------------------------------------------------- workspace
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int workspace(cudaStream_t stream, size_t bytes, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[std::make_pair(dev, stream)];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            e = cudaFreeAsync(w.ptr, stream);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess) return fail(FMHA_ERR_WORKSPACE, "cudaFreeAsync: %s", cudaGetErrorString(e));
+        }
+        e = cudaMallocAsync(&w.ptr, bytes, stream);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return fail(FMHA_ERR_WORKSPACE, "cudaMallocAsync(%zu): %s", bytes, cudaGetErrorString(e));
+        }
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return FMHA_OK;
+}
+
+size_t partial_bytes(long long rows, int hd, int n_splits) {
+    return (size_t)n_splits * (size_t)rows * ((size_t)hd + 1) * sizeof(float);
+}
+
+int run_decode(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
+               float* lse, float* o_part, float* lse_part, bool to_partials, cudaStream_t stream) {
+    DecodeLaunch L;
+    L.q = q;
+    L.o = o;
+    L.lse = lse;
+    L.o_part = o_part;
+    L.lse_part = lse_part;
+    L.to_partials = to_partials;
+    L.p = p;
+    L.sp = sp;
+    L.status = device_status_word();
+    if (!L.status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
+    const int box = decode_kv_tile(p.hd);
+    const long long slabs = (long long)p.batch * p.n_kv_h;
+    int rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, box);
+    if (rc) return rc;
+    rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, box);
+    if (rc) return rc;
+    cudaError_t e = launch_decode(L, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    return FMHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int n_h, int n_kv_h,
+             int T, int s_k, int hd, float scale, int window, int causal, fmha_stream_t stream) {
+    try {
+        Problem p;
+        int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
+        if (rc) return rc;
+        rc = check_inputs(q, k, v, s_k);
+        if (rc) return rc;
+        if (!o || !lse) return fail(FMHA_ERR_NULL, "o and lse must be non-NULL");
+        if (!aligned(o, 16) || !aligned(lse, 4)) return fail(FMHA_ERR_ALIGN, "o must be 16-byte, lse 4-byte aligned");
+        const long long rows = (long long)batch * n_h * T;
+        if (rows == 0) return FMHA_OK;
+        const SplitPlan sp = choose_split(p);
+        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
+        if (sp.n_splits == 1)
+            return run_decode(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
+        void* ws = nullptr;
+        rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits), &ws);
+        if (rc) return rc;
+        float* o_part = static_cast<float*>(ws);
+        float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
+        rc = run_decode(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
+        if (rc) return rc;
+        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+        return FMHA_OK;
+    } catch (...) {
+        return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd");
+    }
+}
+
+int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int window, int causal, int* kv_chunk) {
+    Problem p;
+    int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, 1.0f, window, causal, &p);
+    if (rc) return rc;
+    const SplitPlan sp = choose_split(p);
+    if (kv_chunk) *kv_chunk = sp.kv_chunk;
+    return sp.n_splits;
+}
+
+int fmha_split_layout(int T, int s_k, int window, int kv_chunk, int* first_key) {
+    if (T < 0 || s_k < 0 || window < 0 || kv_chunk < 1)
+        return fail(FMHA_ERR_SHAPE, "fmha_split_layout: need T, s_k, window >= 0 and kv_chunk >= 1");
+    const SplitPlan sp = split_layout(T, s_k, window, kv_chunk);
+    if (first_key) *first_key = sp.kv_begin;
+    return sp.n_splits;
+}
+
+int fmha_fwd_splitkv(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts, int kv_chunk,
+                     int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                     fmha_stream_t stream) {
+    try {
+        Problem p;
+        int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
+        if (rc) return rc;
+        rc = check_inputs(q, k, v, s_k);
+        if (rc) return rc;
+        if (kv_chunk < 1) return fail(FMHA_ERR_SHAPE, "kv_chunk=%d must be >= 1", kv_chunk);
+        if (!o_parts || !lse_parts) return fail(FMHA_ERR_NULL, "o_parts and lse_parts must be non-NULL");
+        if (!aligned(o_parts, 16) || !aligned(lse_parts, 4))
+            return fail(FMHA_ERR_ALIGN, "o_parts must be 16-byte, lse_parts 4-byte aligned");
+        const long long rows = (long long)batch * n_h * T;
+        if (rows == 0) return FMHA_OK;
+        const SplitPlan sp = split_layout(T, s_k, window, kv_chunk);
+        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks (%d)", sp.n_splits);
+        return run_decode(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream);
+    } catch (...) {
+        return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_splitkv");
+    }
+}
+
+int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void* o, float* lse, int batch, int n_h,
+               int T, int hd, fmha_stream_t stream) {
+    if (hd != 64 && hd != 128 && hd != 256 && hd != 512)
+        return fail(FMHA_ERR_HEADDIM, "hd=%d: supported head dims are 64, 128, 256, 512", hd);
+    if (batch < 0 || n_h < 0 || T < 0 || n_splits < 1)
+        return fail(FMHA_ERR_SHAPE, "fmha_merge: need batch, n_h, T >= 0 and n_splits >= 1");
+    const long long rows = (long long)batch * n_h * T;
+    if (rows == 0) return FMHA_OK;
+    if (!o_parts || !lse_parts || !o || !lse) return fail(FMHA_ERR_NULL, "fmha_merge: NULL buffer");
+    if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
+        return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse buffers 4-byte aligned");
+    if ((rows + 7) / 8 > 0x7fffffffLL) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
+    cudaError_t e = launch_merge(o_parts, lse_parts, n_splits, rows, hd, o, lse, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return FMHA_OK;
+}
+
+size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits) {
+    if (batch < 0 || n_h < 0 || T < 0 || hd < 0 || n_splits < 0) return 0;
+    return partial_bytes((long long)batch * n_h * T, hd, n_splits);
+}
+
+int fmha_check_device_status(fmha_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned* w = device_status_word();
+    if (!w) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
+    unsigned h = 0;
+    e = cudaMemcpy(&h, w, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (h) {
+        e = cudaMemset(w, 0, sizeof h);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+        return fail(FMHA_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", h);
+    }
+    return FMHA_OK;
+}
+
+const char* fmha_get_last_error(void) { return g_last_error.c_str(); }
+
+void fmha_release(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+}
+
+int fmha_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// internal.h -- host-side interfaces between the C ABI (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fmha {
+
+// One attention problem, validated by the API layer.
+struct Problem {
+    int batch, n_h, n_kv_h, T, s_k, hd;
+    int window, causal;
+    float scale;
+    int group;  // n_h / n_kv_h
+    int R;      // query rows sharing one KV head: group * T
+};
+
+// Split-KV layout: chunk i covers keys [kv_begin + i*kv_chunk, ... + kv_chunk).
+struct SplitPlan {
+    int kv_begin, kv_chunk, n_splits;
+};
+
+// ---- decode / small-row kernel (decode_kernel.cu) -------------------------
+struct DecodeLaunch {
+    const void* q;
+    void* o;           // bf16 output (n_splits == 1 and !to_partials)
+    float* lse;
+    float* o_part;     // fp32 partial outputs (to_partials)
+    float* lse_part;
+    bool to_partials;
+    CUtensorMap tmap_k, tmap_v;
+    Problem p;
+    SplitPlan sp;
+    unsigned* status;
+};
+int decode_kv_tile(int hd);                  // keys per pipeline stage (TMA box rows)
+int decode_rows_per_cta(int hd, int R);      // query rows per thread block
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
+
+// ---- split-KV merge (merge_kernel.cu) -------------------------------------
+cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows,
+                         int hd, void* o, float* lse, cudaStream_t stream);
+
+// ---- device status word (status.cu) ---------------------------------------
+// Address of the status word on the current device (nullptr on failure).
+unsigned* device_status_word();
+
+}  // namespace fmha

@@ -80,20 +80,29 @@ def sweep():
     return out
 
 
-def make_inputs(w: Workload, seed: int = 0):
-    """(q, k, v) as contiguous CPU bf16 tensors with the workload's shapes."""
-    g = torch.Generator().manual_seed(int(seed))
-    q = torch.randn(w.q_shape(), generator=g, dtype=torch.float32)
-    k = torch.randn(w.kv_shape(), generator=g, dtype=torch.float32)
+def make_inputs(w: Workload, seed: int = 0, device: str = "cpu"):
+    """(q, k, v) as contiguous bf16 tensors with the workload's shapes.
+
+    ``device="cpu"`` draws from the CPU generator; ``device="cuda"`` draws from
+    the CUDA generator (faster for multi-GB shapes).  The two give different
+    numbers for the same seed; a check copies the device tensors to the host so
+    that both sides still read identical bits."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+
+    def draw(shape):
+        return torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+
+    q = draw(w.q_shape()).to(torch.bfloat16)
+    k = draw(w.kv_shape())
     if w.k_mult != 1.0:
-        k = k * w.k_mult
+        k.mul_(w.k_mult)
+    k = k.to(torch.bfloat16)
     if w.v_const_row:
-        c = torch.randn((w.hd,), generator=g, dtype=torch.float32)
-        v = c.expand(w.kv_shape()).contiguous()
+        c = draw((w.hd,))
+        v = c.to(torch.bfloat16).expand(w.kv_shape()).contiguous()
     else:
-        v = torch.randn(w.kv_shape(), generator=g, dtype=torch.float32)
-    return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
-            v.to(torch.bfloat16).contiguous())
+        v = draw(w.kv_shape()).to(torch.bfloat16)
+    return q.contiguous(), k.contiguous(), v.contiguous()
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

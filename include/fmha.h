@@ -1,0 +1,165 @@
+/*
+ * fmha.h -- C ABI of libfmha_gb300.so, the GB300 (sm_103a) fused attention
+ * forward.
+ *
+ * What is computed (per batch b, query head h, query row t):
+ *
+ *     O[b,h,t,:] = softmax_j( scale * <Q[b,h,t,:], K[b,kvh,j,:]> + mask ) V[b,kvh,j,:]
+ *     LSE[b,h,t] = ln sum_{j attended} exp(scale * <Q[b,h,t,:], K[b,kvh,j,:]>)
+ *
+ * with kvh = h / (n_h / n_kv_h).  Sources: the commit pages of the
+ * nvfp4-megamoe-kernel repository (dsv4 directory) and its CURRENT_ISSUE.md
+ * "UMMA FMHA -- Full Pipeline + Production":
+ *   - FA2 online softmax over KV tiles with a running max and sum, P kept
+ *     un-normalised, one final divide by the running sum: commit e4ee9fd,
+ *     multi-tile C API part.
+ *   - scores are the unscaled dot product, the scale is applied in the
+ *     softmax: CURRENT_ISSUE.md, "Key lessons from this session".
+ *   - split-KV partials merged as O = sum_i exp(lse_i) O_i / sum_i exp(lse_i):
+ *     CURRENT_ISSUE.md, "Next steps" item 4.
+ *   - MQA as a K/V head shared by every query head (head stride 0): commit
+ *     e4ee9fd, "Architecture".
+ *   - sliding-window ("D3") and causal ("D4") masks: commit 593bc25, scalar
+ *     reference kernel part.
+ *   - a pure C ABI with no framework types and no host synchronisation on the
+ *     hot path: commit e4ee9fd, multihead C API and "Architecture" parts.
+ *
+ * Readings of points the pages leave open:
+ *   - query row t sits at absolute key position p = s_k - T + t (the T new
+ *     queries follow the s_k - T cached keys: bottom-right alignment);
+ *   - causal: key j is attended iff j <= p;
+ *   - window w > 0: key j is attended iff j > p - w (the last w positions up to
+ *     and including p); w = 0 disables the window;
+ *   - LSE is the natural log of the sum over attended keys of exp(scaled
+ *     score); a row that attends no key gets O = 0 and LSE = -inf.
+ *
+ * Layouts (all contiguous, row-major, device memory owned by the caller):
+ *   Q, O        [batch, n_h,    T,   hd]  bf16 (raw bits, round-to-nearest-even on output)
+ *   K, V        [batch, n_kv_h, s_k, hd]  bf16
+ *   LSE         [batch, n_h,    T]        fp32
+ *   o_parts     [n_splits, batch, n_h, T, hd] fp32   (split-KV partial outputs)
+ *   lse_parts   [n_splits, batch, n_h, T]     fp32
+ *
+ * Accepted shapes: hd in {64, 128, 256, 512}; n_h % n_kv_h == 0;
+ * batch * n_kv_h <= 65535; batch >= 0, T >= 0 (zero means nothing to do);
+ * s_k >= 0; with causal, T <= s_k; window >= 0.  q, k, v, o, o_parts must be
+ * 16-byte aligned, lse and lse_parts 4-byte aligned.
+ *
+ * Errors: every call returns FMHA_OK (0) or a negative FMHA_ERR_* code and
+ * never aborts.  On an argument error nothing is launched.  The message of the
+ * last failure on the calling thread is available from fmha_get_last_error().
+ *
+ * Asynchrony: every compute call is ordered on `stream` (NULL = the legacy
+ * default stream) and returns without synchronising the host.  Kernels bound
+ * every internal wait; a wait that gives up sets a device status word that
+ * fmha_check_device_status() reports.
+ */
+#ifndef FMHA_GB300_H
+#define FMHA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fmha_stream_t;
+
+enum fmha_status {
+    FMHA_OK = 0,
+    FMHA_ERR_NULL = -1,           /* a required pointer is NULL */
+    FMHA_ERR_ALIGN = -2,          /* a pointer is not aligned as required */
+    FMHA_ERR_HEADDIM = -3,        /* hd not in {64, 128, 256, 512} */
+    FMHA_ERR_HEADS = -4,          /* n_h, n_kv_h < 1 or n_h % n_kv_h != 0 */
+    FMHA_ERR_SHAPE = -5,          /* negative size, causal with T > s_k, grid limits, bad window/chunk/scale */
+    FMHA_ERR_WORKSPACE = -6,      /* the internal split-KV workspace could not be allocated */
+    FMHA_ERR_LAUNCH = -7,         /* a CUDA call failed; the message names it */
+    FMHA_ERR_DEVICE_TIMEOUT = -8  /* a kernel's bounded wait gave up (from fmha_check_device_status) */
+};
+
+/*
+ * Fused attention forward.  Writes O (bf16) and LSE (fp32).
+ *
+ * scale: multiplies the raw dot products (usually 1/sqrt(hd)).
+ * window: sliding-window length in keys, 0 = none.  causal: 0 or 1.
+ *
+ * The library chooses whether to split the KV range over several thread
+ * blocks.  When it splits, the fp32 partials live in a workspace the library
+ * allocates on `stream` with cudaMallocAsync the first time a (device,
+ * stream) pair needs more than it holds, and keeps until fmha_release().
+ * Callers that must not allocate use fmha_fwd_splitkv + fmha_merge with their
+ * own buffers.
+ */
+int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+             float scale, int window, int causal, fmha_stream_t stream);
+
+/*
+ * The split-KV plan fmha_fwd uses for this shape: returns the number of
+ * chunks (1 = no split: one kernel writes O and LSE directly; > 1 = a split
+ * pass into the workspace followed by the merge) and stores the chunk length
+ * in *kv_chunk (may be NULL).  Pure host arithmetic apart from reading the
+ * current device's SM count; negative FMHA_ERR_* code on invalid shapes.
+ */
+int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                  int window, int causal, int* kv_chunk);
+
+/*
+ * Split-KV layout for chunks of kv_chunk keys (kv_chunk >= 1): returns the
+ * number of chunks n_splits (>= 1) and stores in *first_key the first key of
+ * chunk 0, which is the first key that query row t = 0 attends (0 without a
+ * window).  Chunk i covers keys [first_key + i*kv_chunk, first_key +
+ * (i+1)*kv_chunk) clipped to s_k.  Pure host arithmetic; returns a negative
+ * FMHA_ERR_* code for invalid arguments.  first_key may be NULL.
+ */
+int fmha_split_layout(int T, int s_k, int window, int kv_chunk, int* first_key);
+
+/*
+ * Split-KV partial pass (the "D5" split of CURRENT_ISSUE.md, "Next steps"
+ * item 4).  For every chunk i of fmha_split_layout(T, s_k, window, kv_chunk)
+ * writes the normalised partial output O_i and its log-sum-exp lse_i over the
+ * keys of that chunk (O_i = 0, lse_i = -inf where the chunk holds no attended
+ * key).  o_parts / lse_parts are caller buffers in the layouts above.
+ */
+int fmha_fwd_splitkv(const void* q, const void* k, const void* v,
+                     float* o_parts, float* lse_parts, int kv_chunk,
+                     int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                     float scale, int window, int causal, fmha_stream_t stream);
+
+/*
+ * Merge split-KV partials (CURRENT_ISSUE.md, "Next steps" item 4):
+ *     LSE = ln sum_i exp(lse_i),   O = sum_i exp(lse_i - LSE) O_i
+ * Partials with lse_i = -inf carry no weight; if all do, O = 0, LSE = -inf.
+ * Writes bf16 O [batch, n_h, T, hd] and fp32 LSE [batch, n_h, T].
+ */
+int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits,
+               void* o, float* lse, int batch, int n_h, int T, int hd,
+               fmha_stream_t stream);
+
+/* Bytes of fp32 partial output (o_parts + lse_parts) that fmha_fwd_splitkv
+ * writes for n_splits chunks. */
+size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns FMHA_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
+ * since the last check, FMHA_ERR_LAUNCH if the synchronisation failed, else
+ * FMHA_OK. */
+int fmha_check_device_status(fmha_stream_t stream);
+
+/* Message for the last non-zero return on the calling thread ("" if none). */
+const char* fmha_get_last_error(void);
+
+/* Frees every workspace fmha_fwd allocated (synchronises each device that
+ * holds one first).  Safe to call at any time no fmha call is in flight. */
+void fmha_release(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int fmha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FMHA_GB300_H */

@@ -1,0 +1,166 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every case draws seeded bf16 inputs, runs the library, runs the oracle on the
+same bits and compares element by element (tolerances in ``check_utils``).
+The named workloads run at their full sizes with the full oracle; the MHA
+shape sweep runs at full size and checks a sample of rows computed one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from check_utils import compare, cosine_per_head, device_inputs, oracle_full, to_np_bits
+from head_attention_forward_fmha_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.Workload
+
+SMALL = [
+    # name, batch, n_h, n_kv_h, T, s_k, hd, window, causal
+    W("s1_tiny_sk1", 1, 1, 1, 1, 1, 64),
+    W("s2_sk_below_tile", 2, 4, 2, 1, 37, 128),
+    W("s3_ragged_tail", 2, 8, 2, 1, 200, 64),
+    W("s4_gqa8", 2, 16, 2, 1, 300, 128),
+    W("s5_mqa_hd256", 1, 16, 1, 1, 129, 256),
+    W("s6_hd512", 1, 4, 4, 1, 100, 512),
+    W("s7_T4_causal", 2, 8, 8, 4, 70, 64, causal=True),
+    W("s8_T3_window", 1, 4, 2, 3, 90, 128, window=17),
+    W("s9_T5_window_causal", 2, 6, 3, 5, 150, 256, window=40, causal=True),
+    W("s10_T32_causal", 1, 4, 4, 32, 96, 128, causal=True),
+    W("s11_T128_causal", 1, 2, 2, 128, 300, 64, causal=True),
+    W("s12_T128_hd512", 1, 2, 2, 128, 130, 512),
+    W("s13_T_gt_sk", 1, 2, 1, 7, 3, 64),
+    W("s14_sk0", 1, 2, 1, 2, 0, 64),  # no cached key at all: O = 0, LSE = -inf
+    W("s15_T17_G3_window_causal", 1, 6, 2, 17, 64, 128, window=8, causal=True),
+    W("s16_window1", 1, 2, 2, 3, 50, 64, window=1, causal=True),
+    W("s17_gqa16_T2", 1, 32, 2, 2, 513, 128, window=300),
+    W("s18_hd256_T128_window", 1, 2, 1, 128, 700, 256, window=100, causal=True),
+    W("s19_long_sk", 1, 4, 1, 1, 5000, 128),
+    W("s20_mqa_G128_hd128", 2, 128, 1, 1, 257, 128),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_fwd_small_shapes(w):
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=1)
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(o, lse, o_ref, lse_ref, w.name)
+    cosine_per_head(o, o_ref, w.name)
+
+
+NAMED = ["single_head_decode", "mqa_decode", "gqa_swa_decode", "causal_prefill"]
+
+
+@pytest.mark.parametrize("name", NAMED)
+def test_fwd_named_workloads_full_oracle(name):
+    w = inputs.WORKLOADS[name]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=0)
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(o, lse, o_ref, lse_ref, name)
+    cosine_per_head(o, o_ref, name)
+
+
+def test_mqa_decode_uniform_v_returns_v():
+    w = inputs.WORKLOADS["mqa_decode_vconst"]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=0)
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale)
+    torch.cuda.synchronize()
+    c = v[0, 0, 0].double().numpy()
+    err = np.abs(o.double().cpu().numpy() - c).max()
+    # P is rounded to bf16 before PV while the sum uses fp32 P: |O - c| <= |c| * 2^-8
+    assert err <= max(1e-2, 2.0 ** -8 * np.abs(c).max()), err
+    _, lse_ref = oracle_full(w, q, k, v)
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+
+
+def test_gqa_swa_decode_split_512_matches_oracle_partials_and_merge():
+    w = inputs.WORKLOADS["gqa_swa_decode"]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=2)
+    op, lp = binding.fmha_fwd_splitkv(qd, kd, vd, 512, scale=w.scale, window=w.window, causal=w.causal)
+    o, lse = binding.fmha_merge(op, lp)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    assert op.shape[0] == 8
+    # partials of two chunks against the oracle restricted to those keys
+    for i in (0, 7):
+        lo = 4096 + 512 * i
+        o_i, l_i = oracle.attention(to_np_bits(q), to_np_bits(k), to_np_bits(v), w.scale, w.window, w.causal,
+                                    key_begin=lo, key_end=lo + 512)
+        compare(op[i], lp[i], o_i, l_i, "partial %d" % i)
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(o, lse, o_ref, lse_ref, "merged")
+    cosine_per_head(o, o_ref, "merged")
+
+
+SPLIT_CASES = [
+    (W("sp1", 1, 4, 2, 1, 40, 64), 1),
+    (W("sp2", 2, 4, 1, 3, 300, 128, window=100, causal=True), 7),
+    (W("sp3", 1, 8, 8, 4, 257, 256, causal=True), 64),
+    (W("sp4", 1, 2, 1, 2, 200, 512), 100),
+    (W("sp5", 1, 16, 2, 1, 129, 128), 129),
+]
+
+
+@pytest.mark.parametrize("w,chunk", SPLIT_CASES, ids=[c[0].name for c in SPLIT_CASES])
+def test_splitkv_partials_and_merge(w, chunk):
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=3)
+    op, lp = binding.fmha_fwd_splitkv(qd, kd, vd, chunk, scale=w.scale, window=w.window, causal=w.causal)
+    o, lse = binding.fmha_merge(op, lp)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    op_ref, lp_ref = oracle.partials(to_np_bits(q), to_np_bits(k), to_np_bits(v), w.scale, chunk, w.window,
+                                     w.causal)
+    assert op.shape[0] == op_ref.shape[0]
+    compare(op, lp, op_ref, lp_ref, w.name + " partials")
+    o_ref, lse_ref = oracle.merge(op_ref, lp_ref)
+    compare(o, lse, o_ref, lse_ref, w.name + " merged")
+    # and the merged result equals the single pass
+    o1, l1 = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+    torch.cuda.synchronize()
+    assert (o1.float() - o.float()).abs().max().item() <= 1.5e-2
+    assert (l1 - lse).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
+def test_merge_kernel_against_oracle(hd):
+    g = torch.Generator().manual_seed(hd)
+    n, b, n_h, T = 5, 2, 3, 4
+    # partial outputs are convex combinations of N(0,1) V rows: |O_i| < 4, where
+    # bf16 rounding of the merged output stays inside the 1.5e-2 bound
+    op = torch.randn((n, b, n_h, T, hd), generator=g).clamp_(-3.9, 3.9)
+    lp = torch.randn((n, b, n_h, T), generator=g) * 3
+    lp[1, 0, 0, 0] = -math.inf          # one empty partial
+    lp[:, 1, 2, 3] = -math.inf          # a row with no key at all
+    op[:, 1, 2, 3] = 0
+    o, lse = binding.fmha_merge(op.cuda(), lp.cuda())
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.merge(op.double().numpy(), lp.double().numpy())
+    compare(o, lse, o_ref, lse_ref, "merge hd%d" % hd)
+
+
+SWEEP = inputs.sweep()
+
+
+@pytest.mark.parametrize("w", SWEEP, ids=[w.name for w in SWEEP])
+def test_sweep_full_size_sampled_rows(w):
+    qd, kd, vd = inputs.make_inputs(w, seed=5, device="cuda")
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    rows = inputs.sample_rows(w, 48, seed=5)
+    o_ref, lse_ref = oracle.attention_rows(to_np_bits(qd), to_np_bits(kd), to_np_bits(vd), rows, w.scale)
+    og = o.reshape(-1, w.hd)[torch.from_numpy(rows).cuda()]
+    lg = lse.reshape(-1)[torch.from_numpy(rows).cuda()]
+    compare(og, lg, o_ref, lse_ref, w.name)
+    del qd, kd, vd, o, lse
+    torch.cuda.empty_cache()
