@@ -33,6 +33,7 @@ SIGNATURES = {
     "fmha_get_last_error": ([], ctypes.c_char_p),
     "fmha_release": ([], None),
     "fmha_version": ([], _i32),
+    "fmha_set_kernel_path": ([_i32], _i32),
 }
 
 _lib = None
@@ -182,3 +183,8 @@ def fmha_release():
 
 def fmha_version():
     return int(load().fmha_version())
+
+
+def fmha_set_kernel_path(path):
+    """0 automatic, 1 decode kernel, 2 tensor-core kernel (where hd <= 256)."""
+    _check(load().fmha_set_kernel_path(int(path)), "fmha_set_kernel_path")

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -139,23 +140,46 @@ int sm_count() {
     return cache[dev];
 }
 
+// ---------------------------------------------------------------- planning
+// Kernel families: the decode kernel (8 or 16 query rows per thread block,
+// mma.sync) and the tensor-core kernel (128 query rows, tcgen05).  A KV head
+// with at least kTcMinRows query rows goes to the tensor-core kernel.
+constexpr int kTcMinRows = 64;
+std::atomic<int> g_path_override{0};  // 0 auto, 1 decode kernel, 2 tensor-core kernel
+
+enum class Path { Decode, TensorCore };
+
+Path choose_path(const Problem& p) {
+    const int ov = g_path_override.load();
+    if (ov == 1 || !tc_supports(p.hd)) return Path::Decode;
+    if (ov == 2) return Path::TensorCore;
+    return p.R >= kTcMinRows ? Path::TensorCore : Path::Decode;
+}
+
+struct KernelShape {
+    int rows_per_cta, kv_tile, ctas_per_sm;
+};
+
+KernelShape kernel_shape(const Problem& p, Path path) {
+    if (path == Path::TensorCore) return {kTcRows, tc_kv_tile(p.hd), 1};
+    return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2};
+}
+
 // Split heuristic: enough thread blocks to fill every SM a few times over,
 // but chunks of at least 256 keys.
 SplitPlan choose_split(const Problem& p) {
-    const int kt = decode_kv_tile(p.hd);
-    const int rows = decode_rows_per_cta(p.hd, p.R);
-    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + rows - 1) / rows);
+    const KernelShape ks = kernel_shape(p, choose_path(p));
+    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + ks.rows_per_cta - 1) / ks.rows_per_cta);
     SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
     const long long span = (long long)p.s_k - whole.kv_begin;
-    const int per_sm = (p.hd == 512) ? 1 : 2;
-    const long long target = 4LL * sm_count() * per_sm;
+    const long long target = 4LL * sm_count() * ks.ctas_per_sm;
     if (units <= 0 || span <= 256 || units >= target) return whole;
     long long n = (target + units - 1) / units;
     const long long max_n = span / 256;
     if (n > max_n) n = max_n;
     if (n <= 1) return whole;
     long long chunk = (span + n - 1) / n;
-    chunk = (chunk + kt - 1) / kt * kt;
+    chunk = (chunk + ks.kv_tile - 1) / ks.kv_tile * ks.kv_tile;
     return split_layout(p.T, p.s_k, p.window, (int)chunk);
 }
 
@@ -195,8 +219,48 @@ size_t partial_bytes(long long rows, int hd, int n_splits) {
     return (size_t)n_splits * (size_t)rows * ((size_t)hd + 1) * sizeof(float);
 }
 
-int run_decode(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
+// Q [slabs, R, hd] viewed as 3-D; boxes of 64 columns x kTcRows rows.
+int make_q_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs) {
+    if (!tensor_map_encoder()) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)R, (cuuint64_t)slabs};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)R * hd * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTcRows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled (Q) failed (CUresult %d)", (int)r);
+    return FMHA_OK;
+}
+
+// Launch the kernel family the plan picks: O/LSE directly, or partials.
+int run_kernel(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
                float* lse, float* o_part, float* lse_part, bool to_partials, cudaStream_t stream) {
+    unsigned* status = device_status_word();
+    if (!status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
+    const Path path = choose_path(p);
+    const KernelShape ks = kernel_shape(p, path);
+    const long long slabs = (long long)p.batch * p.n_kv_h;
+    if (path == Path::TensorCore) {
+        TcLaunch L;
+        L.o = o;
+        L.lse = lse;
+        L.o_part = o_part;
+        L.lse_part = lse_part;
+        L.to_partials = to_partials;
+        L.p = p;
+        L.sp = sp;
+        L.status = status;
+        int rc = make_q_map(&L.tmap_q, q, p.hd, p.R, slabs);
+        if (rc) return rc;
+        rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, ks.kv_tile);
+        if (rc) return rc;
+        rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, ks.kv_tile);
+        if (rc) return rc;
+        cudaError_t e = launch_tc(L, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+        return FMHA_OK;
+    }
     DecodeLaunch L;
     L.q = q;
     L.o = o;
@@ -206,13 +270,10 @@ int run_decode(const void* q, const void* k, const void* v, const Problem& p, co
     L.to_partials = to_partials;
     L.p = p;
     L.sp = sp;
-    L.status = device_status_word();
-    if (!L.status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
-    const int box = decode_kv_tile(p.hd);
-    const long long slabs = (long long)p.batch * p.n_kv_h;
-    int rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, box);
+    L.status = status;
+    int rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, ks.kv_tile);
     if (rc) return rc;
-    rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, box);
+    rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, ks.kv_tile);
     if (rc) return rc;
     cudaError_t e = launch_decode(L, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
@@ -238,13 +299,13 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         const SplitPlan sp = choose_split(p);
         if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
         if (sp.n_splits == 1)
-            return run_decode(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
+            return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
         void* ws = nullptr;
         rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits), &ws);
         if (rc) return rc;
         float* o_part = static_cast<float*>(ws);
         float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
-        rc = run_decode(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
+        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
         if (rc) return rc;
         cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
@@ -288,7 +349,7 @@ int fmha_fwd_splitkv(const void* q, const void* k, const void* v, float* o_parts
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = split_layout(T, s_k, window, kv_chunk);
         if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks (%d)", sp.n_splits);
-        return run_decode(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream);
+        return run_kernel(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream);
     } catch (...) {
         return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_splitkv");
     }
@@ -349,5 +410,11 @@ void fmha_release(void) {
 }
 
 int fmha_version(void) { return 100; }
+
+int fmha_set_kernel_path(int path) {
+    if (path < 0 || path > 2) return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0, 1 or 2 expected (got %d)", path);
+    g_path_override.store(path);
+    return FMHA_OK;
+}
 
 }  // extern "C"

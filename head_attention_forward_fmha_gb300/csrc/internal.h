@@ -38,6 +38,23 @@ int decode_kv_tile(int hd);                  // keys per pipeline stage (TMA box
 int decode_rows_per_cta(int hd, int R);      // query rows per thread block
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 
+// ---- 128-row tensor-core kernel (tc_kernel.cu) ----------------------------
+struct TcLaunch {
+    void* o;
+    float* lse;
+    float* o_part;
+    float* lse_part;
+    bool to_partials;
+    CUtensorMap tmap_q, tmap_k, tmap_v;
+    Problem p;
+    SplitPlan sp;
+    unsigned* status;
+};
+constexpr int kTcRows = 128;                 // query rows per thread block (MMA M)
+bool tc_supports(int hd);
+int tc_kv_tile(int hd);                      // keys per tile (TMA box rows of K and V)
+cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream);
+
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows,
                          int hd, void* o, float* lse, cudaStream_t stream);

@@ -1,0 +1,422 @@
+// tc_kernel.cu -- attention forward for 128-row query tiles on the tcgen05
+// tensor cores (sm_103a).
+//
+// One thread block owns 128 query rows that share one KV head (a causal
+// prefill slice, or the query heads of an MQA/GQA decode step) and one chunk
+// of the KV range.  Both contractions are dense, so both go to the tensor
+// cores:
+//   S_j = Q K_j^T       tcgen05.mma M=128, N=BN, K=hd  (A = Q, B = K; both K-major)
+//   O  += P_j V_j       tcgen05.mma M=128, N=hd, K=BN  (A = P K-major, B = V MN-major)
+// with the accumulators S (two buffers) and O in tensor memory.
+//
+// Warp roles (6 warps):
+//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
+//   warp 1      TMEM owner and MMA issuer (one elected lane)
+//   warps 2..5  softmax: one query row per thread (its TMEM lane); reads S_j
+//               with tcgen05.ld, applies scale and mask, keeps the running max
+//               and sum (FA2 online softmax: commit e4ee9fd of the
+//               nvfp4-megamoe-kernel pages, multi-tile C API part), writes the
+//               un-normalised P_j to shared memory as bf16 and, when the
+//               reference max moved, rescales its O row in TMEM (the O
+//               rescale in registers of commit 593bc25, "D1.5 fix").
+// The reference max only moves when a tile's max exceeds it by more than
+// 2^8, so rescales are rare; P then stays <= 256, exact enough in bf16.
+// Epilogue: O / running sum -> bf16 (or fp32 partials for the split-KV merge),
+// LSE = (max + log2 sum) * ln 2.
+//
+// Every tcgen05.ld/st is executed by all 32 lanes of a warp (they are
+// warp-collective: the TMEM epilogue hang on the 593bc25 page), and TMEM is
+// released with the address tcgen05.alloc returned.
+#include <climits>
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmha {
+namespace {
+
+template <int HD>
+struct TCfg {
+    static constexpr int BM = 128;                     // query rows per CTA (MMA M)
+    static constexpr int BN = (HD <= 128) ? 128 : 64;  // keys per tile
+    static constexpr int STAGES = (HD == 64) ? 3 : 2;
+    static constexpr int NB = HD / 64;                 // 64-column (128-byte) boxes
+    static constexpr int Q_BYTES = BM * HD * 2;
+    static constexpr int KV_TILE = BN * HD * 2;        // one K or V tile
+    static constexpr int P_BYTES = BM * BN * 2;
+    static constexpr int THREADS = 192;
+    static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
+    static constexpr int O_COL = 2 * BN;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int OFF_P = OFF_V + STAGES * KV_TILE;
+    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int N_BARS = 1 + 3 * STAGES + 2 + 2;
+    static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
+    static_assert(O_COL + HD <= TMEM_COLS, "S double buffer + O must fit in TMEM");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct TcArgs {
+    __nv_bfloat16* o;
+    float* lse;
+    float* o_part;
+    float* lse_part;
+    int to_partials;
+    int n_h, n_kv_h, T, s_k, group, R, window, causal;
+    float scale_log2;
+    int kv_begin, kv_chunk;
+    long long rows_total;
+    unsigned* status;
+};
+
+__device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, int& hi) {
+    const int p = a.s_k - a.T + t;
+    lo = 0;
+    hi = a.s_k - 1;
+    if (a.causal) hi = min(hi, p);
+    if (a.window > 0) lo = max(lo, p - a.window + 1);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const TcArgs a) {
+    using C = TCfg<HD>;
+    constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sq = smem + C::OFF_Q;
+    uint8_t* sk = smem + C::OFF_K;
+    uint8_t* sv = smem + C::OFF_V;
+    uint8_t* sp = smem + C::OFF_P;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* v_full = k_full + ST;
+    uint64_t* kv_empty = v_full + ST;
+    uint64_t* s_full = kv_empty + ST;  // [2]
+    uint64_t* p_ready = s_full + 2;
+    uint64_t* o_done = p_ready + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rt = blockIdx.x, split = blockIdx.y, slab = blockIdx.z;
+    const int b = slab / a.n_kv_h, kvh = slab - b * a.n_kv_h;
+    const long long row0 = ((long long)b * a.n_h + (long long)kvh * a.group) * a.T;  // slab's first query row
+    const int r_begin = rt * BM;
+    const int r_end = min(a.R, r_begin + BM);
+
+    // KV range of this CTA: its chunk intersected with what its rows attend.
+    const int c_lo = a.kv_begin + split * a.kv_chunk;
+    const int c_hi = min(a.s_k, c_lo + a.kv_chunk);
+    int u_lo, u_hi;
+    if (r_end - r_begin >= a.T) {
+        int l0, h0, l1, h1;
+        attended_rows(0, a, l0, h0);
+        attended_rows(a.T - 1, a, l1, h1);
+        u_lo = l0;
+        u_hi = h1;
+    } else {
+        int l0, h0, l1, h1;
+        attended_rows(r_begin % a.T, a, l0, h0);
+        attended_rows((r_end - 1) % a.T, a, l1, h1);
+        // rows r_begin..r_end-1 may wrap once past t = T-1
+        if ((r_end - 1) % a.T < r_begin % a.T) {
+            int lz, hz, lx, hx;
+            attended_rows(0, a, lz, hz);
+            attended_rows(a.T - 1, a, lx, hx);
+            u_lo = lz;
+            u_hi = hx;
+        } else {
+            u_lo = l0;
+            u_hi = h1;
+        }
+    }
+    const int k_lo = max(c_lo, u_lo), k_hi = min(c_hi, u_hi + 1);
+    const int n_tiles = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_ready, 128);
+        mbar_init(o_done, 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
+            const uint64_t pol = l2_policy_evict_first();
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % ST;
+                if (j >= ST && !mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, a.status)) break;
+                const int key = k_lo + j * BN;
+                mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
+#pragma unroll
+                for (int c = 0; c < C::NB; ++c)
+                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, key, slab, &k_full[s], pol);
+                mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
+#pragma unroll
+                for (int c = 0; c < C::NB; ++c)
+                    tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, key, slab, &v_full[s], pol);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, 1);
+            const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk), v_addr = smem_u32(sv),
+                           p_addr = smem_u32(sp);
+            bool ok = mbar_wait(q_full, 0, a.status);
+            auto issue_qk = [&](int j) -> bool {
+                const int s = j % ST;
+                if (!mbar_wait(&k_full[s], (j / ST) & 1, a.status)) return false;
+                tc_fence_after();
+                const uint32_t d = tmem + C::S_COL0 + (j & 1) * BN;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes into the swizzled row
+                    const uint64_t ad = smem_desc_sw128(q_addr + (kk >> 2) * BM * 128 + off, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(k_addr + s * C::KV_TILE + (kk >> 2) * BN * 128 + off, 16, 1024);
+                    tc_mma_f16(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[j & 1]);
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int s = j % ST;
+                if (j + 1 < n_tiles && !issue_qk(j + 1)) break;
+                if (!mbar_wait(p_ready, j & 1, a.status)) break;
+                if (!mbar_wait(&v_full[s], (j / ST) & 1, a.status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, BN * 128, 1024);
+                    tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(o_done);
+                tc_commit(&kv_empty[s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;              // TMEM lane and tile row
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int grow = r_begin + row;
+        const bool valid = grow < r_end;
+        int jlo = INT_MAX, jhi = -1;
+        if (valid) {
+            attended_rows(grow % a.T, a, jlo, jhi);
+            jlo = max(jlo, c_lo);
+            jhi = min(jhi, c_hi - 1);
+        }
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                float v32[32];
+                tmem_ld32(t_lane + C::S_COL0 + (j & 1) * BN + c * 32, v32);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
+            }
+            tmem_wait_ld();
+            const int key0 = k_lo + j * BN;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                const int key = key0 + i;
+                x[i] = (key >= jlo && key <= jhi) ? x[i] * a.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, x[i]);
+            }
+            float alpha = 1.f;
+            float m_new = m_ref;
+            if (mt > m_ref + 8.f) {
+                m_new = mt;
+                alpha = exp2f(m_ref - m_new);  // 0 when m_ref = -inf
+            }
+            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+            // PV_{j-1} must be complete before P is overwritten and O rescaled.
+            if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int g = 0; g < BN / 64; ++g) {
+                uint8_t* prow = sp + g * BM * 128 + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pv[e] = exp2f(x[g * 64 + ch * 8 + e] - mu);
+                        rs += pv[e];
+                    }
+                    uint4 pk;
+                    pk.x = pack_bf16x2(pv[0], pv[1]);
+                    pk.y = pack_bf16x2(pv[2], pv[3]);
+                    pk.z = pack_bf16x2(pv[4], pv[5]);
+                    pk.w = pack_bf16x2(pv[6], pv[7]);
+                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
+                }
+            }
+            l = l * alpha + rs;
+            m_ref = m_new;
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    tmem_st32(t_lane + C::O_COL + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_ready);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+        tc_fence_after();
+        constexpr float kLn2 = 0.693147180559945309f;
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        const long long gr = row0 + grow;
+        const long long prow = (long long)split * a.rows_total + gr;
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                float ov[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+                }
+                if (!valid) continue;
+                if (!a.to_partials) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + gr * HD + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                        pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                        pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                        pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                        dst[q] = pk;
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(a.o_part + prow * HD + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
+                                             ov[q * 4 + 3] * inv);
+                }
+            }
+            if (valid) {
+                if (!a.to_partials)
+                    a.lse[gr] = lse;
+                else
+                    a.lse_part[prow] = lse;
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int HD>
+cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
+    using C = TCfg<HD>;
+    auto kern = fwd_tc_kernel<HD>;
+    static bool attr_set[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 128) attr_set[dev] = true;
+    }
+    TcArgs a;
+    a.o = static_cast<__nv_bfloat16*>(L.o);
+    a.lse = L.lse;
+    a.o_part = L.o_part;
+    a.lse_part = L.lse_part;
+    a.to_partials = L.to_partials ? 1 : 0;
+    a.n_h = L.p.n_h;
+    a.n_kv_h = L.p.n_kv_h;
+    a.T = L.p.T;
+    a.s_k = L.p.s_k;
+    a.group = L.p.group;
+    a.R = L.p.R;
+    a.window = L.p.window;
+    a.causal = L.p.causal;
+    a.scale_log2 = (float)((double)L.p.scale * 1.4426950408889634);
+    a.kv_begin = L.sp.kv_begin;
+    a.kv_chunk = L.sp.kv_chunk;
+    a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
+    a.status = L.status;
+    dim3 grid((L.p.R + C::BM - 1) / C::BM, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_kv_tile(int hd) { return hd <= 128 ? 128 : 64; }
+
+bool tc_supports(int hd) { return hd == 64 || hd == 128 || hd == 256; }
+
+cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream) {
+    switch (L.p.hd) {
+        case 64: return launch_t<64>(L, stream);
+        case 128: return launch_t<128>(L, stream);
+        case 256: return launch_t<256>(L, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fmha

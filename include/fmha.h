@@ -155,6 +155,16 @@ const char* fmha_get_last_error(void);
  * holds one first).  Safe to call at any time no fmha call is in flight. */
 void fmha_release(void);
 
+/*
+ * Kernel-family selection for every later call in the process: 0 = automatic
+ * (default: the 128-row tensor-core kernel when a KV head has at least 64
+ * query rows and hd <= 256, else the decode kernel), 1 = always the decode
+ * kernel, 2 = the tensor-core kernel wherever hd <= 256.  Meant for tests and
+ * measurements that compare the two families on one shape; results agree
+ * within the documented tolerance.  Returns FMHA_ERR_SHAPE for other values.
+ */
+int fmha_set_kernel_path(int path);
+
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int fmha_version(void);
 

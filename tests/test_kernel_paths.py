@@ -1,0 +1,84 @@
+"""GPU parity of each kernel family on shapes the automatic choice would send
+to the other one: the decode kernel (mma.sync, 8/16 query rows per block) and
+the 128-row tensor-core kernel (tcgen05 + TMEM), both against the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from check_utils import compare, cosine_per_head, device_inputs, oracle_full, to_np_bits
+from head_attention_forward_fmha_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.Workload
+
+SHAPES = [
+    W("k1_decode_gqa8", 2, 16, 2, 1, 300, 128),
+    W("k2_T1_hd64", 3, 4, 4, 1, 1000, 64),
+    W("k3_T128_causal_hd64", 1, 2, 2, 128, 300, 64, causal=True),
+    W("k4_T128_causal_hd128", 2, 2, 1, 128, 520, 128, causal=True),
+    W("k5_T128_causal_hd256", 1, 4, 4, 128, 512, 256, causal=True),
+    W("k6_T100_window_causal", 1, 2, 2, 100, 333, 128, window=77, causal=True),
+    W("k7_mqa_G128_hd128", 2, 128, 1, 1, 700, 128),
+    W("k8_mqa_G128_hd256", 1, 128, 1, 1, 257, 256),
+    W("k9_gqa_prefill_G4_T40", 1, 8, 2, 40, 200, 128, causal=True),
+    W("k10_R200_two_tiles", 1, 200, 1, 1, 129, 64),
+    W("k11_T64_no_mask_sk1", 1, 2, 2, 64, 1, 128),
+    W("k12_sk0", 1, 2, 2, 70, 0, 64),
+    W("k13_T_gt_sk", 1, 2, 2, 90, 40, 256),
+    W("k14_window_only_T128", 1, 2, 1, 128, 1000, 64, window=200),
+    W("k15_long_sk_T64", 1, 1, 1, 64, 4097, 128, causal=True),
+]
+
+
+@pytest.fixture
+def path():
+    yield binding.fmha_set_kernel_path
+    binding.fmha_set_kernel_path(0)
+
+
+@pytest.mark.parametrize("which", [1, 2], ids=["decode_kernel", "tensor_core_kernel"])
+@pytest.mark.parametrize("w", SHAPES, ids=[w.name for w in SHAPES])
+def test_kernel_family_matches_oracle(w, which, path):
+    path(which)
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=4)
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(o, lse, o_ref, lse_ref, "%s/path%d" % (w.name, which))
+    cosine_per_head(o, o_ref, "%s/path%d" % (w.name, which))
+
+
+@pytest.mark.parametrize("chunk", [64, 100, 256])
+def test_tensor_core_kernel_partials(chunk, path):
+    path(2)
+    w = W("tc_split", 1, 4, 2, 64, 500, 128, window=300, causal=True)
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=6)
+    op, lp = binding.fmha_fwd_splitkv(qd, kd, vd, chunk, scale=w.scale, window=w.window, causal=w.causal)
+    o, lse = binding.fmha_merge(op, lp)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    op_ref, lp_ref = oracle.partials(to_np_bits(q), to_np_bits(k), to_np_bits(v), w.scale, chunk, w.window,
+                                     w.causal)
+    compare(op, lp, op_ref, lp_ref, "tc partials chunk %d" % chunk)
+    o_ref, lse_ref = oracle.merge(op_ref, lp_ref)
+    compare(o, lse, o_ref, lse_ref, "tc merged chunk %d" % chunk)
+
+
+def test_causal_prefill_both_families_agree(path):
+    w = inputs.WORKLOADS["causal_prefill"]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=8)
+    outs = []
+    for which in (1, 2):
+        path(which)
+        o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, causal=True)
+        torch.cuda.synchronize()
+        outs.append((o.float(), lse))
+    binding.fmha_check_device_status()
+    assert (outs[0][0] - outs[1][0]).abs().max().item() <= 1.5e-2
+    assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-3
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(outs[1][0], outs[1][1], o_ref, lse_ref, "causal_prefill tc")
