@@ -103,25 +103,34 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
-def csrc_digest():
+# Source files each kernel is built from: a recorded ncu traffic figure is
+# only used while these files are unchanged.
+KERNEL_SOURCES = {
+    "decode_splitkv": ("decode_kernel.cu", "ptx.cuh"),
+    "fwd_tc": ("tc_kernel.cu", "ptx.cuh"),
+    "fwd_tc_wide": ("tc_wide_kernel.cu", "ptx.cuh"),
+    "merge_lse": ("merge_kernel.cu", "ptx.cuh"),
+}
+
+
+def kernel_digest(kernel):
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(CSRC, name), "rb").read())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update(open(os.path.join(CSRC, name), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_tag, workload):
+def recorded_traffic(kernel, workload):
     """DRAM bytes per launch recorded from an ncu capture in profiles/, or None
     if absent or taken on other kernel sources."""
-    path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel_tag, workload))
+    path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel, workload))
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    d = re.search(r"csrc_digest:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != csrc_digest():
+    d = re.search(r"kernel_sources_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_digest(kernel):
         return None
     return float(m.group(1))
 
@@ -267,8 +276,9 @@ def max_over_ranks(x, dist):
 # ----------------------------------------------------------------------------
 def measure_kernel_only(binding, w, sets, stream, steps):
     """Average duration of each kernel of the plan, timed alone (ms per launch)."""
-    n_splits, chunk = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal)
-    out = {"n_splits": n_splits, "kv_chunk": chunk}
+    n_splits, chunk, kernel = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window,
+                                                    w.causal, with_kernel=True)
+    out = {"n_splits": n_splits, "kv_chunk": chunk, "kernel": kernel}
     if n_splits == 1:
         def fwd(i):
             q, k, v, o, lse = sets[i]
@@ -467,15 +477,16 @@ def main():
                 "frac_bf16_peak": round(f2 / (r2["ms_per_step"] * 1e-3) / 1e12 / bf16_peak, 4),
                 "frac_attainable": round(max(b2 / (hbm_peak * 1e9), f2 / (bf16_peak * 1e12)) /
                                          (r2["ms_per_step"] * 1e-3), 4),
-                "n_splits": r2["n_splits"], "kv_chunk": r2["kv_chunk"],
-                "decode_kernel_ms": round(r2["decode_ms"], 5), "merge_kernel_ms": round(r2["merge_ms"], 5),
+                "n_splits": r2["n_splits"], "kv_chunk": r2["kv_chunk"], "kernel": r2["kernel"],
+                "kernel_ms": round(r2["decode_ms"], 5), "merge_kernel_ms": round(r2["merge_ms"], 5),
+                "traffic": recorded_traffic(r2["kernel"], name),
                 "steps": st,
             }
     sampler.stop()
 
     n = world
     value = n * bytes_step / (res["ms_per_step"] * 1e-3) / 1e9
-    traffic = recorded_traffic("decode_splitkv", w.name)
+    traffic = recorded_traffic(res["kernel"], w.name)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 6), "higher_is_better": True,
@@ -487,8 +498,9 @@ def main():
                          % (res["n_sets"], res["n_sets"] * bytes_step / 1e6, res["l2_bytes"] / 1e6),
                    "timing": "CUDA graphs of fmha_fwd calls, CUDA events on the launching stream",
                    "n_splits": res["n_splits"], "kv_chunk": res["kv_chunk"]},
-        "roofline": roofline_obj(bytes_step, res["decode_ms"], hbm_peak, peak_kind, traffic),
-        "kernels_ms": {"decode_splitkv": round(res["decode_ms"], 6), "merge_lse": round(res["merge_ms"], 6)},
+        "roofline": dict(roofline_obj(bytes_step, res["decode_ms"], hbm_peak, peak_kind, traffic),
+                         kernel=res["kernel"]),
+        "kernels_ms": {res["kernel"]: round(res["decode_ms"], 6), "merge_lse": round(res["merge_ms"], 6)},
         "tflops": round(algo_flops(w) / (res["ms_per_step"] * 1e-3) / 1e12, 2),
         "e2e": {"value": round(bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},

@@ -23,7 +23,8 @@ ERRORS = {
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fmha_fwd": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
-    "fmha_fwd_plan": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
+    "fmha_fwd_plan": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)],
+                      _i32),
     "fmha_split_layout": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
     "fmha_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp],
                          _i32),
@@ -35,6 +36,7 @@ SIGNATURES = {
     "fmha_version": ([], _i32),
     "fmha_set_kernel_path": ([_i32], _i32),
 }
+
 
 _lib = None
 
@@ -113,11 +115,18 @@ def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stre
     return o, lse
 
 
-def fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, window=0, causal=False):
-    """(n_splits, kv_chunk) that fmha_fwd uses for this shape."""
-    chunk = ctypes.c_int(0)
-    n = load().fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, int(window), int(bool(causal)), ctypes.byref(chunk))
+KERNELS = {1: "decode_splitkv", 2: "fwd_tc", 3: "fwd_tc_wide"}
+
+
+def fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, window=0, causal=False, with_kernel=False):
+    """(n_splits, kv_chunk) that fmha_fwd uses for this shape, plus the kernel
+    family name if ``with_kernel``."""
+    chunk, kern = ctypes.c_int(0), ctypes.c_int(0)
+    n = load().fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, int(window), int(bool(causal)), ctypes.byref(chunk),
+                             ctypes.byref(kern))
     _check(n if n < 0 else 0, "fmha_fwd_plan")
+    if with_kernel:
+        return n, chunk.value, KERNELS.get(kern.value, "?")
     return n, chunk.value
 
 
@@ -188,3 +197,4 @@ def fmha_version():
 def fmha_set_kernel_path(path):
     """0 automatic, 1 decode kernel, 2 tensor-core kernel (where hd <= 256)."""
     _check(load().fmha_set_kernel_path(int(path)), "fmha_set_kernel_path")
+

@@ -147,35 +147,49 @@ int sm_count() {
 constexpr int kTcMinRows = 64;
 std::atomic<int> g_path_override{0};  // 0 auto, 1 decode kernel, 2 tensor-core kernel
 
-enum class Path { Decode, TensorCore };
+enum class Path { Decode, TensorCore, TensorCoreWide };
 
 Path choose_path(const Problem& p) {
     const int ov = g_path_override.load();
-    if (ov == 1 || !tc_supports(p.hd)) return Path::Decode;
-    if (ov == 2) return Path::TensorCore;
-    return p.R >= kTcMinRows ? Path::TensorCore : Path::Decode;
+    const bool tc_ok = tc_supports(p.hd) || p.hd == 512;
+    if (ov == 1 || !tc_ok) return Path::Decode;
+    if (ov == 2 || p.R >= kTcMinRows) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
+    return Path::Decode;
 }
 
 struct KernelShape {
-    int rows_per_cta, kv_tile, ctas_per_sm;
+    int rows_per_cta, kv_tile, ctas_per_sm, blocks_per_row_tile, min_chunk;
 };
 
 KernelShape kernel_shape(const Problem& p, Path path) {
-    if (path == Path::TensorCore) return {kTcRows, tc_kv_tile(p.hd), 1};
-    return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2};
+    if (path == Path::TensorCore) return {kTcRows, tc_kv_tile(p.hd), 1, 1, 256};
+    if (path == Path::TensorCoreWide) return {kTcRows, tc_wide_kv_tile(), 1, 2, 128};
+    return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2, 1, 256};
 }
 
-// Split heuristic: enough thread blocks to fill every SM a few times over,
-// but chunks of at least 256 keys.
+// Split heuristic.  Decode kernel: enough thread blocks to fill every SM a few
+// times over (its partials are small next to the K/V it streams).  Tensor-core
+// kernels: split only when the row tiles cannot fill half the GPU, and then
+// only up to one wave, since their fp32 partials (128 rows x hd per chunk)
+// cost about as much traffic as the K/V chunk itself.
 SplitPlan choose_split(const Problem& p) {
-    const KernelShape ks = kernel_shape(p, choose_path(p));
-    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + ks.rows_per_cta - 1) / ks.rows_per_cta);
+    const Path path = choose_path(p);
+    const KernelShape ks = kernel_shape(p, path);
+    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + ks.rows_per_cta - 1) / ks.rows_per_cta) *
+                            ks.blocks_per_row_tile;
     SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
     const long long span = (long long)p.s_k - whole.kv_begin;
-    const long long target = 4LL * sm_count() * ks.ctas_per_sm;
-    if (units <= 0 || span <= 256 || units >= target) return whole;
+    const long long sms = sm_count();
+    long long target;
+    if (path != Path::Decode) {
+        if (units * 2 >= sms) return whole;
+        target = sms;
+    } else {
+        target = 4LL * sms * ks.ctas_per_sm;
+    }
+    if (units <= 0 || span <= ks.min_chunk || units >= target) return whole;
     long long n = (target + units - 1) / units;
-    const long long max_n = span / 256;
+    const long long max_n = span / ks.min_chunk;
     if (n > max_n) n = max_n;
     if (n <= 1) return whole;
     long long chunk = (span + n - 1) / n;
@@ -241,7 +255,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
     const Path path = choose_path(p);
     const KernelShape ks = kernel_shape(p, path);
     const long long slabs = (long long)p.batch * p.n_kv_h;
-    if (path == Path::TensorCore) {
+    if (path != Path::Decode) {
         TcLaunch L;
         L.o = o;
         L.lse = lse;
@@ -257,7 +271,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         if (rc) return rc;
         rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, ks.kv_tile);
         if (rc) return rc;
-        cudaError_t e = launch_tc(L, stream);
+        cudaError_t e = (path == Path::TensorCoreWide) ? launch_tc_wide(L, stream) : launch_tc(L, stream);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
         return FMHA_OK;
     }
@@ -315,12 +329,17 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     }
 }
 
-int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int window, int causal, int* kv_chunk) {
+int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int window, int causal, int* kv_chunk,
+                  int* kernel) {
     Problem p;
     int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, 1.0f, window, causal, &p);
     if (rc) return rc;
     const SplitPlan sp = choose_split(p);
     if (kv_chunk) *kv_chunk = sp.kv_chunk;
+    if (kernel) {
+        const Path path = choose_path(p);
+        *kernel = path == Path::Decode ? 1 : (path == Path::TensorCore ? 2 : 3);
+    }
     return sp.n_splits;
 }
 

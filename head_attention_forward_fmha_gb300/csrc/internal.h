@@ -54,6 +54,10 @@ constexpr int kTcRows = 128;                 // query rows per thread block (MMA
 bool tc_supports(int hd);
 int tc_kv_tile(int hd);                      // keys per tile (TMA box rows of K and V)
 cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream);
+// hd = 512 variant (tc_wide_kernel.cu): two thread blocks per row tile, one
+// per half of the head dim of O.
+int tc_wide_kv_tile();
+cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
 
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows,

@@ -1,0 +1,415 @@
+// tc_wide_kernel.cu -- tcgen05 attention forward for hd = 512 (128-row tiles).
+//
+// At hd 512 the fp32 O accumulator of a 128-row tile (128 x 512 x 4 bytes)
+// fills all of tensor memory, and the bf16 Q tile alone is 128 KB of shared
+// memory.  So each thread block owns 128 query rows, one KV chunk and one HALF
+// of the head dim of O (256 columns; blockIdx.x = 2 * row_tile + half):
+//   S_j  = sum_c Q[:, c] K_j[:, c]^T   over the 8 64-column chunks c of hd
+//          (every block computes the full S; it is cheap next to the loads)
+//   O_h += P_j V_j[:, 256h : 256h + 256]
+// Q and K stream through one ring of 16 KB slots chunk by chunk (Q chunks
+// come from L2 after the first block reads them), then the four 64-column V
+// chunks of this half.  TMEM: two S buffers (2 x 128 columns) + O half (256).
+// Softmax, lazy rescale and the epilogue are those of tc_kernel.cu; both
+// halves compute identical (max, sum), and half 0 writes the LSE.
+#include <climits>
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmha {
+namespace {
+
+struct WCfg {
+    static constexpr int HD = 512;
+    static constexpr int HALF = 256;
+    static constexpr int BM = 128;
+    static constexpr int BN = 128;
+    static constexpr int SLOT_BYTES = 128 * 128;       // 128 rows x 64 bf16 columns
+    static constexpr int NSLOT = 8;
+    static constexpr int QK_ITEMS = 2 * (HD / 64);     // Q chunk + K chunk per column block
+    static constexpr int V_ITEMS = HALF / 64;
+    static constexpr int P_BYTES = BM * BN * 2;
+    static constexpr int THREADS = 192;
+    static constexpr int O_COL = 2 * BN;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_P = NSLOT * SLOT_BYTES;
+    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int N_BARS = 2 * NSLOT + 2 + 2;
+    static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
+    static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct WideArgs {
+    __nv_bfloat16* o;
+    float* lse;
+    float* o_part;
+    float* lse_part;
+    int to_partials;
+    int n_h, n_kv_h, T, s_k, group, R, window, causal;
+    float scale_log2;
+    int kv_begin, kv_chunk;
+    long long rows_total;
+    unsigned* status;
+};
+
+__device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, int& hi) {
+    const int p = a.s_k - a.T + t;
+    lo = 0;
+    hi = a.s_k - 1;
+    if (a.causal) hi = min(hi, p);
+    if (a.window > 0) lo = max(lo, p - a.window + 1);
+}
+
+__global__ void __launch_bounds__(WCfg::THREADS, 1)
+    fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const WideArgs a) {
+    using C = WCfg;
+    constexpr int BM = C::BM, BN = C::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem + C::OFF_RING;
+    uint8_t* sp = smem + C::OFF_P;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* slot_full = bars;
+    uint64_t* slot_empty = bars + C::NSLOT;
+    uint64_t* s_full = slot_empty + C::NSLOT;  // [2]
+    uint64_t* p_ready = s_full + 2;
+    uint64_t* o_done = p_ready + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rt = blockIdx.x >> 1, half = blockIdx.x & 1;
+    const int split = blockIdx.y, slab = blockIdx.z;
+    const int b = slab / a.n_kv_h, kvh = slab - b * a.n_kv_h;
+    const long long row0 = ((long long)b * a.n_h + (long long)kvh * a.group) * a.T;
+    const int r_begin = rt * BM;
+    const int r_end = min(a.R, r_begin + BM);
+
+    const int c_lo = a.kv_begin + split * a.kv_chunk;
+    const int c_hi = min(a.s_k, c_lo + a.kv_chunk);
+    int u_lo, u_hi;
+    {
+        int t0, t1;
+        if (r_end - r_begin >= a.T || (r_end - 1) % a.T < r_begin % a.T) {
+            t0 = 0;
+            t1 = a.T - 1;
+        } else {
+            t0 = r_begin % a.T;
+            t1 = (r_end - 1) % a.T;
+        }
+        int l0, h0, l1, h1;
+        w_attended(t0, a, l0, h0);
+        w_attended(t1, a, l1, h1);
+        u_lo = l0;
+        u_hi = h1;
+    }
+    const int k_lo = max(c_lo, u_lo), k_hi = min(c_hi, u_hi + 1);
+    const int n_tiles = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_ready, 128);
+        mbar_init(o_done, 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // Item order: QK(0), then for each tile j: QK(j+1), V(j) -- the order
+        // the MMA warp consumes them in.
+        if (lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            int item = 0;
+            bool ok = true;
+            auto slot_acquire = [&](int& s) -> bool {
+                s = item % C::NSLOT;
+                if (item >= C::NSLOT && !mbar_wait(&slot_empty[s], ((item / C::NSLOT) - 1) & 1, a.status))
+                    return false;
+                ++item;
+                return true;
+            };
+            auto load_qk = [&](int j) -> bool {
+                const int key = k_lo + j * BN;
+                for (int c = 0; c < C::HD / 64; ++c) {
+                    int s;
+                    if (!slot_acquire(s)) return false;
+                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
+                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, &slot_full[s], pol_q);
+                    if (!slot_acquire(s)) return false;
+                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
+                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
+                }
+                return true;
+            };
+            auto load_v = [&](int j) -> bool {
+                const int key = k_lo + j * BN;
+                for (int c = 0; c < C::V_ITEMS; ++c) {
+                    int s;
+                    if (!slot_acquire(s)) return false;
+                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
+                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmv, half * C::HALF + c * 64, key, slab,
+                                     &slot_full[s], pol_kv);
+                }
+                return true;
+            };
+            ok = load_qk(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles) ok = load_qk(j + 1);
+                if (ok) ok = load_v(j);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, 64, 1);
+            const uint32_t ring_addr = smem_u32(ring), p_addr = smem_u32(sp);
+            int item = 0;
+            bool ok = true;
+            auto slot_take = [&](int& s) -> bool {
+                s = item % C::NSLOT;
+                if (!mbar_wait(&slot_full[s], (item / C::NSLOT) & 1, a.status)) return false;
+                ++item;
+                return true;
+            };
+            auto issue_qk = [&](int j) -> bool {
+                const uint32_t d = tmem + (j & 1) * BN;
+                for (int c = 0; c < C::HD / 64; ++c) {
+                    int sq, sk;
+                    if (!slot_take(sq) || !slot_take(sk)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(ring_addr + sq * C::SLOT_BYTES + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(ring_addr + sk * C::SLOT_BYTES + kk * 32, 16, 1024);
+                        tc_mma_f16(d, ad, bd, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&slot_empty[sq]);
+                    tc_commit(&slot_empty[sk]);
+                }
+                tc_commit(&s_full[j & 1]);
+                return true;
+            };
+            ok = issue_qk(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
+                if (!(ok = mbar_wait(p_ready, j & 1, a.status))) break;
+                tc_fence_after();
+                for (int c = 0; c < C::V_ITEMS && ok; ++c) {
+                    int sv;
+                    if (!(ok = slot_take(sv))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t ad =
+                            smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(ring_addr + sv * C::SLOT_BYTES + kk * 16 * 128,
+                                                            BN * 128, 1024);
+                        tc_mma_f16(tmem + C::O_COL + c * 64, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&slot_empty[sv]);
+                }
+                if (ok) tc_commit(o_done);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int grow = r_begin + row;
+        const bool valid = grow < r_end;
+        int jlo = INT_MAX, jhi = -1;
+        if (valid) {
+            w_attended(grow % a.T, a, jlo, jhi);
+            jlo = max(jlo, c_lo);
+            jhi = min(jhi, c_hi - 1);
+        }
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                float v32[32];
+                tmem_ld32(t_lane + (j & 1) * BN + c * 32, v32);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
+            }
+            tmem_wait_ld();
+            const int key0 = k_lo + j * BN;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                const int key = key0 + i;
+                x[i] = (key >= jlo && key <= jhi) ? x[i] * a.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, x[i]);
+            }
+            float alpha = 1.f, m_new = m_ref;
+            if (mt > m_ref + 8.f) {
+                m_new = mt;
+                alpha = exp2f(m_ref - m_new);
+            }
+            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+            if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int g = 0; g < BN / 64; ++g) {
+                uint8_t* prow = sp + g * BM * 128 + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pv[e] = exp2f(x[g * 64 + ch * 8 + e] - mu);
+                        rs += pv[e];
+                    }
+                    uint4 pk;
+                    pk.x = pack_bf16x2(pv[0], pv[1]);
+                    pk.y = pack_bf16x2(pv[2], pv[3]);
+                    pk.z = pack_bf16x2(pv[4], pv[5]);
+                    pk.w = pack_bf16x2(pv[6], pv[7]);
+                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
+                }
+            }
+            l = l * alpha + rs;
+            m_ref = m_new;
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < C::HALF / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    tmem_st32(t_lane + C::O_COL + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_ready);
+        }
+        if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+        tc_fence_after();
+        constexpr float kLn2 = 0.693147180559945309f;
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        const long long gr = row0 + grow;
+        const long long prow = (long long)split * a.rows_total + gr;
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < C::HALF / 32; ++c) {
+                float ov[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+                }
+                if (!valid) continue;
+                const int col = half * C::HALF + c * 32;
+                if (!a.to_partials) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + gr * C::HD + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                        pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                        pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                        pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                        dst[q] = pk;
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(a.o_part + prow * C::HD + col);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
+                                             ov[q * 4 + 3] * inv);
+                }
+            }
+            if (valid && half == 0) {
+                if (!a.to_partials)
+                    a.lse[gr] = lse;
+                else
+                    a.lse_part[prow] = lse;
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+int tc_wide_kv_tile() { return WCfg::BN; }
+
+cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
+    using C = WCfg;
+    static bool attr_set[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(fwd_tc_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 128) attr_set[dev] = true;
+    }
+    WideArgs a;
+    a.o = static_cast<__nv_bfloat16*>(L.o);
+    a.lse = L.lse;
+    a.o_part = L.o_part;
+    a.lse_part = L.lse_part;
+    a.to_partials = L.to_partials ? 1 : 0;
+    a.n_h = L.p.n_h;
+    a.n_kv_h = L.p.n_kv_h;
+    a.T = L.p.T;
+    a.s_k = L.p.s_k;
+    a.group = L.p.group;
+    a.R = L.p.R;
+    a.window = L.p.window;
+    a.causal = L.p.causal;
+    a.scale_log2 = (float)((double)L.p.scale * 1.4426950408889634);
+    a.kv_begin = L.sp.kv_begin;
+    a.kv_chunk = L.sp.kv_chunk;
+    a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
+    a.status = L.status;
+    dim3 grid(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
+    fwd_tc_wide_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, a);
+    return cudaGetLastError();
+}
+
+}  // namespace fmha

@@ -97,14 +97,16 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              float scale, int window, int causal, fmha_stream_t stream);
 
 /*
- * The split-KV plan fmha_fwd uses for this shape: returns the number of
- * chunks (1 = no split: one kernel writes O and LSE directly; > 1 = a split
- * pass into the workspace followed by the merge) and stores the chunk length
- * in *kv_chunk (may be NULL).  Pure host arithmetic apart from reading the
- * current device's SM count; negative FMHA_ERR_* code on invalid shapes.
+ * The plan fmha_fwd uses for this shape: returns the number of KV chunks
+ * (1 = no split: one kernel writes O and LSE directly; > 1 = a split pass
+ * into the workspace followed by the merge), stores the chunk length in
+ * *kv_chunk and the kernel family in *kernel (1 = decode kernel, 2 =
+ * tensor-core kernel, 3 = tensor-core kernel for hd 512); either pointer may
+ * be NULL.  Pure host arithmetic apart from reading the current device's SM
+ * count; negative FMHA_ERR_* code on invalid shapes.
  */
 int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
-                  int window, int causal, int* kv_chunk);
+                  int window, int causal, int* kv_chunk, int* kernel);
 
 /*
  * Split-KV layout for chunks of kv_chunk keys (kv_chunk >= 1): returns the
@@ -157,9 +159,9 @@ void fmha_release(void);
 
 /*
  * Kernel-family selection for every later call in the process: 0 = automatic
- * (default: the 128-row tensor-core kernel when a KV head has at least 64
- * query rows and hd <= 256, else the decode kernel), 1 = always the decode
- * kernel, 2 = the tensor-core kernel wherever hd <= 256.  Meant for tests and
+ * (default: the 128-row tensor-core kernels when a KV head has at least 64
+ * query rows, else the decode kernel), 1 = always the decode kernel, 2 =
+ * always the tensor-core kernels.  Meant for tests and
  * measurements that compare the two families on one shape; results agree
  * within the documented tolerance.  Returns FMHA_ERR_SHAPE for other values.
  */

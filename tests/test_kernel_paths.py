@@ -30,6 +30,10 @@ SHAPES = [
     W("k13_T_gt_sk", 1, 2, 2, 90, 40, 256),
     W("k14_window_only_T128", 1, 2, 1, 128, 1000, 64, window=200),
     W("k15_long_sk_T64", 1, 1, 1, 64, 4097, 128, causal=True),
+    W("k16_mqa_G128_hd512", 2, 128, 1, 1, 300, 512),
+    W("k17_T128_causal_hd512", 1, 2, 2, 128, 260, 512, causal=True),
+    W("k18_hd512_G64_T2_window", 1, 64, 1, 2, 700, 512, window=300),
+    W("k19_hd512_R200", 1, 200, 1, 1, 129, 512),
 ]
 
 
@@ -52,10 +56,10 @@ def test_kernel_family_matches_oracle(w, which, path):
     cosine_per_head(o, o_ref, "%s/path%d" % (w.name, which))
 
 
-@pytest.mark.parametrize("chunk", [64, 100, 256])
-def test_tensor_core_kernel_partials(chunk, path):
+@pytest.mark.parametrize("hd,chunk", [(128, 64), (128, 100), (128, 256), (512, 128), (512, 200)])
+def test_tensor_core_kernel_partials(hd, chunk, path):
     path(2)
-    w = W("tc_split", 1, 4, 2, 64, 500, 128, window=300, causal=True)
+    w = W("tc_split", 1, 4, 2, 64, 500, hd, window=300, causal=True)
     (q, k, v), (qd, kd, vd) = device_inputs(w, seed=6)
     op, lp = binding.fmha_fwd_splitkv(qd, kd, vd, chunk, scale=w.scale, window=w.window, causal=w.causal)
     o, lse = binding.fmha_merge(op, lp)
@@ -63,9 +67,9 @@ def test_tensor_core_kernel_partials(chunk, path):
     binding.fmha_check_device_status()
     op_ref, lp_ref = oracle.partials(to_np_bits(q), to_np_bits(k), to_np_bits(v), w.scale, chunk, w.window,
                                      w.causal)
-    compare(op, lp, op_ref, lp_ref, "tc partials chunk %d" % chunk)
+    compare(op, lp, op_ref, lp_ref, "tc partials hd %d chunk %d" % (hd, chunk))
     o_ref, lse_ref = oracle.merge(op_ref, lp_ref)
-    compare(o, lse, o_ref, lse_ref, "tc merged chunk %d" % chunk)
+    compare(o, lse, o_ref, lse_ref, "tc merged hd %d chunk %d" % (hd, chunk))
 
 
 def test_causal_prefill_both_families_agree(path):
