@@ -35,7 +35,10 @@ SIGNATURES = {
     "fmha_release": ([], None),
     "fmha_version": ([], _i32),
     "fmha_set_kernel_path": ([_i32], _i32),
+    "fmha_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
 }
+# Size of the fixed split-KV scratch fmha_fwd_noalloc uses (FMHA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 _lib = None
@@ -198,3 +201,16 @@ def fmha_set_kernel_path(path):
     """0 automatic, 1 decode kernel, 2 tensor-core kernel (where hd <= 256)."""
     _check(load().fmha_set_kernel_path(int(path)), "fmha_set_kernel_path")
 
+
+def fmha_fwd_noalloc(q, k, v, o, lse, scale=None, window=0, causal=False, stream=None):
+    """fmha_fwd for callers that cannot allocate device memory: O and LSE must be
+    given, and split-KV partials use the library's fixed scratch array instead
+    of a workspace (see include/fmha.h)."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd_noalloc(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                                 b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)),
+                                 _stream(stream))
+    _check(rc, "fmha_fwd_noalloc")
+    return o, lse

@@ -437,3 +437,73 @@ int fmha_set_kernel_path(int path) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation entry point
+// fmha_fwd_noalloc: the same computation as fmha_fwd for callers that cannot
+// allocate device memory.  Its split-KV partials live in the file-scope array
+// below instead of a workspace from cudaMallocAsync.  In host code the array's
+// name is only a host-side stand-in, so the device address is looked up once
+// per device with cudaGetSymbolAddress (with that device current) and passed
+// to the kernels.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FMHA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxNoallocDevices = 128;
+void* g_noalloc_addr[kMaxNoallocDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxNoallocDevices) return fail(FMHA_ERR_LAUNCH, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-allocation scratch");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return FMHA_OK;
+}
+
+}  // namespace
+
+extern "C" int fmha_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int n_h,
+                                int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                                fmha_stream_t stream) {
+    try {
+        Problem p;
+        int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
+        if (rc) return rc;
+        rc = check_inputs(q, k, v, s_k);
+        if (rc) return rc;
+        if (!o || !lse) return fail(FMHA_ERR_NULL, "o and lse must be non-NULL");
+        if (!aligned(o, 16) || !aligned(lse, 4)) return fail(FMHA_ERR_ALIGN, "o must be 16-byte, lse 4-byte aligned");
+        const long long rows = (long long)batch * n_h * T;
+        if (rows == 0) return FMHA_OK;
+        const SplitPlan sp = choose_split(p);
+        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
+        if (sp.n_splits == 1) return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
+        const size_t need = partial_bytes(rows, hd, sp.n_splits);
+        if (need > (size_t)FMHA_NOALLOC_SCRATCH_BYTES)
+            return fail(FMHA_ERR_WORKSPACE,
+                        "fmha_fwd_noalloc: this shape needs %zu bytes of split-KV scratch (%d chunks x %lld rows); "
+                        "the fixed scratch holds %zu bytes",
+                        need, sp.n_splits, rows, (size_t)FMHA_NOALLOC_SCRATCH_BYTES);
+        void* scratch = nullptr;
+        rc = noalloc_scratch(&scratch);
+        if (rc) return rc;
+        float* o_part = static_cast<float*>(scratch);
+        float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
+        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
+        if (rc) return rc;
+        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+        return FMHA_OK;
+    } catch (...) {
+        return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_noalloc");
+    }
+}

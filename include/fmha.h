@@ -167,6 +167,40 @@ void fmha_release(void);
  */
 int fmha_set_kernel_path(int path);
 
+/*
+ * fmha_fwd_noalloc -- fmha_fwd for callers that cannot allocate device memory.
+ * (This entry point has no counterpart on the pages the method comes from.)
+ *
+ * Some callers must not allocate: an inference runtime that reserves all of
+ * its device memory up front and accounts for every byte, code that runs on a
+ * strict memory budget, or a hot loop that must not risk the synchronisation
+ * and latency that cudaMalloc/cudaFree (or a pool growing) can bring.  For
+ * them this call computes exactly what fmha_fwd computes, with the same plan
+ * and the same kernels, and calls no allocating routine: when the plan splits
+ * the KV range, the fp32 partials go to one fixed scratch array of
+ * FMHA_NOALLOC_SCRATCH_BYTES (32 MiB) that is part of the library's device
+ * image, so every GPU that loads the library holds it until the process exits.
+ *
+ * - A shape whose partials (fmha_splitkv_workspace_bytes for fmha_fwd_plan's
+ *   chunk count) exceed the scratch is rejected with FMHA_ERR_WORKSPACE and a
+ *   message naming both sizes; nothing is launched.  Shapes that fmha_fwd_plan
+ *   does not split need no scratch at all.
+ * - The first call on each device looks up the scratch's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one scratch array, which keeps the last
+ *   call's contents.  Nothing in it needs to start at zero: each call writes
+ *   every partial before its merge reads it.  Calls whose work overlaps on the
+ *   GPU (for example on two streams without ordering between them) race on the
+ *   scratch and may return wrong results; order them on one stream or with
+ *   events.
+ * Arguments, layouts and errors are those of fmha_fwd.
+ */
+#define FMHA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fmha_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                     float scale, int window, int causal, fmha_stream_t stream);
+
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int fmha_version(void);
 
