@@ -9,9 +9,12 @@
 //   O  += P_j V_j       tcgen05.mma M=128, N=hd, K=BN  (A = P K-major, B = V MN-major)
 // with the accumulators S (two buffers) and O in tensor memory.
 //
-// Warp roles (6 warps):
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
-//   warp 1      TMEM owner and MMA issuer (one elected lane)
+// Warp roles (7 warps):
+//   warp 0      TMA producer for Q (once) and K_j; a K stage is released as
+//               soon as QK_j has read it
+//   warp 6      TMA producer for V_j; a V stage is released after PV_j
+//   warp 1      TMEM owner and MMA issuer (one elected lane): QK runs two
+//               tiles ahead of PV (S is double-buffered), P is double-buffered
 //   warps 2..5  softmax: one query row per thread (its TMEM lane); reads S_j
 //               with tcgen05.ld, applies scale and mask, keeps the running max
 //               and sum (FA2 online softmax: commit e4ee9fd of the
@@ -38,21 +41,22 @@ template <int HD>
 struct TCfg {
     static constexpr int BM = 128;                     // query rows per CTA (MMA M)
     static constexpr int BN = (HD <= 128) ? 128 : 64;  // keys per tile
-    static constexpr int STAGES = (HD == 64) ? 3 : 2;
+    static constexpr int KST = (HD == 64) ? 4 : 2;     // K stages
+    static constexpr int VST = (HD == 64) ? 4 : 2;     // V stages
     static constexpr int NB = HD / 64;                 // 64-column (128-byte) boxes
     static constexpr int Q_BYTES = BM * HD * 2;
     static constexpr int KV_TILE = BN * HD * 2;        // one K or V tile
-    static constexpr int P_BYTES = BM * BN * 2;
-    static constexpr int THREADS = 192;
+    static constexpr int P_BYTES = BM * BN * 2;        // one P buffer (two are kept)
+    static constexpr int THREADS = 224;
     static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
     static constexpr int O_COL = 2 * BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
-    static constexpr int OFF_P = OFF_V + STAGES * KV_TILE;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int N_BARS = 1 + 3 * STAGES + 2 + 2;
+    static constexpr int OFF_V = OFF_K + KST * KV_TILE;
+    static constexpr int OFF_P = OFF_V + VST * KV_TILE;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2;
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HD <= TMEM_COLS, "S double buffer + O must fit in TMEM");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -84,7 +88,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const TcArgs a) {
     using C = TCfg<HD>;
-    constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES;
+    constexpr int BM = C::BM, BN = C::BN, KST = C::KST, VST = C::VST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sq = smem + C::OFF_Q;
@@ -94,11 +98,12 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* v_full = k_full + ST;
-    uint64_t* kv_empty = v_full + ST;
-    uint64_t* s_full = kv_empty + ST;  // [2]
-    uint64_t* p_ready = s_full + 2;
-    uint64_t* o_done = p_ready + 1;
+    uint64_t* k_empty = k_full + KST;
+    uint64_t* v_full = k_empty + KST;
+    uint64_t* v_empty = v_full + VST;
+    uint64_t* s_full = v_empty + VST;  // [2] by S buffer
+    uint64_t* p_ready = s_full + 2;    // [2] by P buffer
+    uint64_t* o_done = p_ready + 2;    // [2] by P buffer: PV of a tile using that P buffer completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,15 +144,19 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_empty[s], 1);
         }
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(p_ready, 128);
-        mbar_init(o_done, 1);
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(&s_full[b2], 1);
+            mbar_init(&p_ready[b2], 128);
+            mbar_init(&o_done[b2], 1);
+        }
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -160,31 +169,42 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ Q / K producer
         if (lane == 0 && n_tiles > 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
             mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
             const uint64_t pol = l2_policy_evict_first();
             for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % ST;
-                if (j >= ST && !mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, a.status)) break;
-                const int key = k_lo + j * BN;
+                const int s = j % KST;
+                if (j >= KST && !mbar_wait(&k_empty[s], ((j / KST) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c)
-                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, key, slab, &k_full[s], pol);
+                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, k_lo + j * BN, slab,
+                                     &k_full[s], pol);
+            }
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ V producer
+        if (lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tmv);
+            const uint64_t pol = l2_policy_evict_first();
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % VST;
+                if (j >= VST && !mbar_wait(&v_empty[s], ((j / VST) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c)
-                    tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, key, slab, &v_full[s], pol);
+                    tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, k_lo + j * BN, slab,
+                                     &v_full[s], pol);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order: QK_0, QK_1, then per tile j: PV_j, QK_{j+2}.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, 1);
@@ -192,8 +212,8 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                            p_addr = smem_u32(sp);
             bool ok = mbar_wait(q_full, 0, a.status);
             auto issue_qk = [&](int j) -> bool {
-                const int s = j % ST;
-                if (!mbar_wait(&k_full[s], (j / ST) & 1, a.status)) return false;
+                const int s = j % KST;
+                if (!mbar_wait(&k_full[s], (j / KST) & 1, a.status)) return false;
                 tc_fence_after();
                 const uint32_t d = tmem + C::S_COL0 + (j & 1) * BN;
 #pragma unroll
@@ -204,23 +224,27 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                     tc_mma_f16(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[j & 1]);
+                tc_commit(&k_empty[s]);
                 return true;
             };
             if (ok) ok = issue_qk(0);
+            if (ok && n_tiles > 1) ok = issue_qk(1);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int s = j % ST;
-                if (j + 1 < n_tiles && !issue_qk(j + 1)) break;
-                if (!mbar_wait(p_ready, j & 1, a.status)) break;
-                if (!mbar_wait(&v_full[s], (j / ST) & 1, a.status)) break;
+                const int s = j % VST;
+                const int pb = j & 1;
+                if (!mbar_wait(&p_ready[pb], (j >> 1) & 1, a.status)) break;
+                if (!mbar_wait(&v_full[s], (j / VST) & 1, a.status)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t ad = smem_desc_sw128(p_addr + pb * C::P_BYTES + (kk >> 2) * BM * 128 + (kk & 3) * 32,
+                                                        16, 1024);
                     const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, BN * 128, 1024);
                     tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(o_done);
-                tc_commit(&kv_empty[s]);
+                tc_commit(&o_done[pb]);
+                tc_commit(&v_empty[s]);
+                if (j + 2 < n_tiles && !issue_qk(j + 2)) break;
             }
         }
     } else {
@@ -239,6 +263,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
+            const int pb = j & 1;
             if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status)) {
                 ok = false;
                 break;
@@ -268,23 +293,34 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 alpha = exp2f(m_ref - m_new);  // 0 when m_ref = -inf
             }
             const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-            // PV_{j-1} must be complete before P is overwritten and O rescaled.
-            if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
-                ok = false;
-                break;
-            }
+            // Exponentials and the row sum before waiting on the tensor core.
             float rs = 0.f;
 #pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                x[i] = exp2f(x[i] - mu);
+                rs += x[i];
+            }
+            l = l * alpha + rs;
+            m_ref = m_new;
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+            // P buffer pb was last read by PV_{j-2}; a rescale of O needs PV_{j-1} done.
+            if (rescale) {
+                if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status)) {
+                    ok = false;
+                    break;
+                }
+            } else if (j >= 2) {
+                if (!mbar_wait(&o_done[pb], ((j >> 1) - 1) & 1, a.status)) {
+                    ok = false;
+                    break;
+                }
+            }
+#pragma unroll
             for (int g = 0; g < BN / 64; ++g) {
-                uint8_t* prow = sp + g * BM * 128 + row * 128;
+                uint8_t* prow = sp + pb * C::P_BYTES + g * BM * 128 + row * 128;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        pv[e] = exp2f(x[g * 64 + ch * 8 + e] - mu);
-                        rs += pv[e];
-                    }
+                    const float* pv = x + g * 64 + ch * 8;
                     uint4 pk;
                     pk.x = pack_bf16x2(pv[0], pv[1]);
                     pk.y = pack_bf16x2(pv[2], pv[3]);
@@ -293,9 +329,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                     *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
                 }
             }
-            l = l * alpha + rs;
-            m_ref = m_new;
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
@@ -310,10 +344,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_ready);
+            mbar_arrive(&p_ready[pb]);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+        if (ok && n_tiles > 0) ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
         tc_fence_after();
         constexpr float kLn2 = 0.693147180559945309f;
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
