@@ -246,14 +246,20 @@ def graph_time(step_fn, n_sets, steps, stream, per_graph=None):
     return e0.elapsed_time(e1)
 
 
-def dist_setup(args):
+def dist_setup(args, backend="nccl"):
+    """(world, rank, local_rank, torch.distributed or None).  One process per
+    GPU; ranks are independent replicas (no data-path collective), the process
+    group only carries the barrier and the max-over-ranks timing."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
         return ws, rank, local, dist
     return 1, 0, 0, None
 
@@ -266,9 +272,16 @@ def barrier(dist):
 def max_over_ranks(x, dist):
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step, ms_per_step, world):
+    """Whole-job throughput: every rank processes its own batch; the slowest
+    rank's step time (already maxed over ranks) bounds the job."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------------------
@@ -485,7 +498,7 @@ def main():
     sampler.stop()
 
     n = world
-    value = n * bytes_step / (res["ms_per_step"] * 1e-3) / 1e9
+    value = aggregate_gbs(bytes_step, res["ms_per_step"], n)
     traffic = recorded_traffic(res["kernel"], w.name)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": n, "steps": args.steps,

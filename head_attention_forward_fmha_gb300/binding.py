@@ -35,6 +35,7 @@ SIGNATURES = {
     "fmha_release": ([], None),
     "fmha_version": ([], _i32),
     "fmha_set_kernel_path": ([_i32], _i32),
+    "fmha_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i32),
     "fmha_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
 }
 # Size of the fixed split-KV scratch fmha_fwd_noalloc uses (FMHA_NOALLOC_SCRATCH_BYTES).
@@ -195,6 +196,11 @@ def fmha_release():
 
 def fmha_version():
     return int(load().fmha_version())
+
+
+def fmha_selftest_wait_timeout(timeout_us, stream=None):
+    """Launch the bounded-wait self-test kernel (see include/fmha.h)."""
+    _check(load().fmha_selftest_wait_timeout(int(timeout_us), _stream(stream)), "fmha_selftest_wait_timeout")
 
 
 def fmha_set_kernel_path(path):

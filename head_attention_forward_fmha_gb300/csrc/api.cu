@@ -385,7 +385,7 @@ int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void*
     if (!o_parts || !lse_parts || !o || !lse) return fail(FMHA_ERR_NULL, "fmha_merge: NULL buffer");
     if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
         return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse buffers 4-byte aligned");
-    if ((rows + 7) / 8 > 0x7fffffffLL) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
+    if (rows > (1LL << 32)) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
     cudaError_t e = launch_merge(o_parts, lse_parts, n_splits, rows, hd, o, lse, stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FMHA_OK;
@@ -429,6 +429,14 @@ void fmha_release(void) {
 }
 
 int fmha_version(void) { return 100; }
+
+int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream) {
+    if (timeout_us < 1 || timeout_us > 10000000u)
+        return fail(FMHA_ERR_SHAPE, "timeout_us must be in [1, 10^7] (got %u)", timeout_us);
+    cudaError_t e = launch_wait_timeout_selftest((unsigned long long)timeout_us * 1000ull, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "wait-timeout self-test launch");
+    return FMHA_OK;
+}
 
 int fmha_set_kernel_path(int path) {
     if (path < 0 || path > 2) return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0, 1 or 2 expected (got %d)", path);

@@ -66,5 +66,7 @@ cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_spl
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).
 unsigned* device_status_word();
+// Launch a kernel whose bounded wait must time out after limit_ns.
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace fmha

@@ -4,9 +4,10 @@
 // item 4: O = sum_i exp(lse_i) O_i / sum_i exp(lse_i).  Evaluated with the
 // exponents shifted by max_i lse_i:
 //     LSE = M + ln sum_i exp(lse_i - M),   O = sum_i exp(lse_i - LSE) O_i.
-// One warp per output row; each lane owns HD/32 consecutive columns, so a
-// warp reads one contiguous fp32 row of every partial (coalesced 8-32 B per
-// lane) and writes one bf16 row.
+// One warp per (output row, slice of up to 128 columns): the lanes first
+// share the chunk weights (lane i holds chunk i's weight), then stream the
+// slice of every partial with coalesced 8- or 16-byte loads, several chunks
+// in flight, and write one bf16 slice.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -16,18 +17,39 @@ namespace {
 constexpr int kMergeWarps = 8;
 
 template <int HD>
+struct MCfg {
+    static constexpr int VEC = (HD >= 128) ? 4 : 2;  // fp32 columns per lane
+    static constexpr int SLICE = 32 * VEC;            // columns per warp
+    static constexpr int NSLICE = HD / SLICE;
+};
+
+template <int VEC>
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[VEC]) {
+    if constexpr (VEC == 4) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    } else {
+        const float2 u = __ldg(reinterpret_cast<const float2*>(p));
+        v[0] = u.x; v[1] = u.y;
+    }
+}
+
+template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n_splits,
                      long long rows, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
-    constexpr int V = HD / 32;  // columns per lane: 2, 4, 8 or 16
+    using C = MCfg<HD>;
+    constexpr int V = C::VEC;
     const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-    if (row >= rows) return;
+    const long long task = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (task >= rows * C::NSLICE) return;
+    const long long row = task / C::NSLICE;
+    const int col = (int)(task - row * C::NSLICE) * C::SLICE + lane * V;
     constexpr float kLog2e = 1.4426950408889634f;
     constexpr float kLn2 = 0.693147180559945309f;
 
     float mx = -INFINITY;
-    for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, lse_parts[(long long)i * rows + row]);
+    for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, __ldg(lse_parts + (long long)i * rows + row));
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
 
@@ -36,39 +58,57 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     for (int e = 0; e < V; ++e) acc[e] = 0.f;
     float den = 0.f;
     if (mx != -INFINITY) {
-        for (int i = 0; i < n_splits; ++i) {
-            const float li = lse_parts[(long long)i * rows + row];
-            const float w = exp2f((li - mx) * kLog2e);  // 0 for an empty partial
-            den += w;
-            const float* src = o_parts + ((long long)i * rows + row) * HD + lane * V;
-            if constexpr (V == 2) {
-                const float2 u = *reinterpret_cast<const float2*>(src);
-                acc[0] += w * u.x;
-                acc[1] += w * u.y;
-            } else {
+        for (int base = 0; base < n_splits; base += 32) {
+            // lane i: weight of chunk base + i (0 for an empty chunk or past the end)
+            const int mine = base + lane;
+            const float w_mine =
+                (mine < n_splits) ? exp2f((__ldg(lse_parts + (long long)mine * rows + row) - mx) * kLog2e) : 0.f;
+            float wsum = w_mine;
 #pragma unroll
-                for (int e = 0; e < V; e += 4) {
-                    const float4 u = *reinterpret_cast<const float4*>(src + e);
-                    acc[e] += w * u.x;
-                    acc[e + 1] += w * u.y;
-                    acc[e + 2] += w * u.z;
-                    acc[e + 3] += w * u.w;
-                }
+            for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+            den += wsum;
+            const int cnt = min(32, n_splits - base);
+            int i = 0;
+            for (; i + 4 <= cnt; i += 4) {
+                float v0[V], v1[V], v2[V], v3[V];
+                load_vec<V>(o_parts + ((long long)(base + i) * rows + row) * HD + col, v0);
+                load_vec<V>(o_parts + ((long long)(base + i + 1) * rows + row) * HD + col, v1);
+                load_vec<V>(o_parts + ((long long)(base + i + 2) * rows + row) * HD + col, v2);
+                load_vec<V>(o_parts + ((long long)(base + i + 3) * rows + row) * HD + col, v3);
+                const float w0 = __shfl_sync(0xffffffffu, w_mine, i);
+                const float w1 = __shfl_sync(0xffffffffu, w_mine, i + 1);
+                const float w2 = __shfl_sync(0xffffffffu, w_mine, i + 2);
+                const float w3 = __shfl_sync(0xffffffffu, w_mine, i + 3);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] += w0 * v0[e] + w1 * v1[e] + w2 * v2[e] + w3 * v3[e];
+            }
+            for (; i < cnt; ++i) {
+                float v0[V];
+                load_vec<V>(o_parts + ((long long)(base + i) * rows + row) * HD + col, v0);
+                const float w0 = __shfl_sync(0xffffffffu, w_mine, i);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] += w0 * v0[e];
             }
         }
     }
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
-    __nv_bfloat16* dst = o + row * HD + lane * V;
-#pragma unroll
-    for (int e = 0; e < V; e += 2)
-        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-    if (lane == 0) lse[row] = (den > 0.f) ? mx + log2f(den) * kLn2 : -INFINITY;
+    __nv_bfloat16* dst = o + row * HD + col;
+    if constexpr (V == 4) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0 && col == 0) lse[row] = (den > 0.f) ? mx + log2f(den) * kLn2 : -INFINITY;
 }
 
 template <int HD>
 cudaError_t launch_t(const float* o_parts, const float* lse_parts, int n_splits, long long rows, void* o,
                      float* lse, cudaStream_t stream) {
-    const long long blocks = (rows + kMergeWarps - 1) / kMergeWarps;
+    const long long tasks = rows * MCfg<HD>::NSLICE;
+    const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     merge_lse_kernel<HD><<<(unsigned)blocks, kMergeWarps * 32, 0, stream>>>(
         o_parts, lse_parts, n_splits, rows, static_cast<__nv_bfloat16*>(o), lse);
     return cudaGetLastError();

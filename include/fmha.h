@@ -158,6 +158,17 @@ const char* fmha_get_last_error(void);
 void fmha_release(void);
 
 /*
+ * Failure-detection self-test: launches one thread that waits, through the
+ * same bounded mbarrier wait the attention kernels use, on a barrier phase
+ * that nothing completes.  After timeout_us microseconds (1 .. 10^7) the wait
+ * gives up, sets the device status word and the kernel returns normally, so
+ * the next fmha_check_device_status() on this device returns
+ * FMHA_ERR_DEVICE_TIMEOUT and the context stays usable.  No fault, trap or
+ * hang is involved.
+ */
+int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream);
+
+/*
  * Kernel-family selection for every later call in the process: 0 = automatic
  * (default: the 128-row tensor-core kernels when a KV head has at least 64
  * query rows, else the decode kernel), 1 = always the decode kernel, 2 =
