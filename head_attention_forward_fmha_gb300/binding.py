@@ -11,7 +11,9 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libfmha_gb300.so")
+# FMHA_GB300_LIB may name another build of the same library (for example one
+# compiled with different tile parameters) to load instead of the in-tree one.
+LIB_PATH = os.environ.get("FMHA_GB300_LIB") or os.path.join(_PKG, "libfmha_gb300.so")
 
 FMHA_OK = 0
 ERRORS = {

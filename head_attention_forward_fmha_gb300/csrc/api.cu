@@ -233,17 +233,20 @@ size_t partial_bytes(long long rows, int hd, int n_splits) {
     return (size_t)n_splits * (size_t)rows * ((size_t)hd + 1) * sizeof(float);
 }
 
-// Q [slabs, R, hd] viewed as 3-D; boxes of 64 columns x kTcRows rows.
-int make_q_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs) {
+// A row-tile tensor [slabs, R, hd] (Q, O, or fp32 partials) viewed as 3-D;
+// boxes of 128 bytes of columns x kTcRows rows, 128-byte swizzle.
+int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs, bool f32, const char* what) {
     if (!tensor_map_encoder()) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+    const int esz = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)R, (cuuint64_t)slabs};
-    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)R * hd * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTcRows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * esz, (cuuint64_t)R * hd * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kTcRows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled (Q) failed (CUresult %d)", (int)r);
+    CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled (%s) failed (CUresult %d)", what, (int)r);
     return FMHA_OK;
 }
 
@@ -265,7 +268,10 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.p = p;
         L.sp = sp;
         L.status = status;
-        int rc = make_q_map(&L.tmap_q, q, p.hd, p.R, slabs);
+        int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, false, "Q");
+        if (rc) return rc;
+        rc = to_partials ? make_rows_map(&L.tmap_o, o_part, p.hd, p.R, slabs * sp.n_splits, true, "O partials")
+                         : make_rows_map(&L.tmap_o, o, p.hd, p.R, slabs, false, "O");
         if (rc) return rc;
         rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, ks.kv_tile);
         if (rc) return rc;

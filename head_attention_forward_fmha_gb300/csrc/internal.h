@@ -46,6 +46,7 @@ struct TcLaunch {
     float* lse_part;
     bool to_partials;
     CUtensorMap tmap_q, tmap_k, tmap_v;
+    CUtensorMap tmap_o;  // bf16 O [slabs, R, hd] (box 64 x 128), or fp32 partials [n_splits*slabs, R, hd] (box 32 x 128)
     Problem p;
     SplitPlan sp;
     unsigned* status;

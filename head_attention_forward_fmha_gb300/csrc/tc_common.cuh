@@ -1,0 +1,146 @@
+// tc_common.cuh -- pieces shared by the tcgen05 kernels (tc_kernel.cu and
+// tc_wide_kernel.cu): the per-row online-softmax step, the write of P into the
+// K-major 128-byte-swizzled operand layout, and the TMA-store epilogue.
+#pragma once
+#include "ptx.cuh"
+
+namespace fmha {
+
+// One row's S tile (raw dot products, x[BN]) -> un-normalised probabilities
+// in place, updating the running reference max m_ref and sum l (FA2 online
+// softmax: commit e4ee9fd of the nvfp4-megamoe-kernel pages, multi-tile C API
+// part).  Keys outside [jlo, jhi] are masked.  sl2 = scale * log2(e).
+// The reference max only moves when the tile's max exceeds it by more than
+// 8 (log2 units); then alpha = 2^(m_old - m_new) and the caller rescales O.
+// Probabilities are therefore <= 2^8.
+template <int BN>
+__device__ __forceinline__ void softmax_row_tile(float (&x)[BN], int key0, int jlo, int jhi, float sl2, float& m_ref,
+                                                 float& l, float& alpha) {
+    const bool full = key0 >= jlo && key0 + BN - 1 <= jhi;
+    float mt, mul;
+    if (sl2 > 0.f) {
+        // max(sl2 * x) = sl2 * max(x): scale once, fold it into the exponent's FMA
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                const int key = key0 + i;
+                x[i] = (key >= jlo && key <= jhi) ? x[i] : -INFINITY;
+                m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+            }
+        }
+        const float mr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mt = (mr == -INFINITY) ? -INFINITY : mr * sl2;
+        mul = sl2;
+    } else {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+            const int key = key0 + i;
+            x[i] = (key >= jlo && key <= jhi) ? x[i] * sl2 : -INFINITY;
+            m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+        }
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mul = 1.f;
+    }
+    alpha = 1.f;
+    float m_new = m_ref;
+    if (mt > m_ref + 8.f) {
+        m_new = mt;
+        alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
+    }
+    const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < BN; ++i) {
+        x[i] = ex2_approx(fmaf(x[i], mul, -mu));  // masked keys: 2^-inf = 0
+        s4[i & 3] += x[i];
+    }
+    l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+    m_ref = m_new;
+}
+
+// Row `row` of P (BN bf16 values) into the A-operand layout: groups of 64 keys,
+// each a 128-row x 128-byte K-major tile with the 128-byte swizzle (16-byte
+// chunk c of row r stored at chunk c ^ (r % 8)).
+template <int BN>
+__device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float (&x)[BN]) {
+    constexpr int GROUPS = (BN + 63) / 64;
+    constexpr int CHUNKS = (BN < 64 ? BN : 64) / 8;
+#pragma unroll
+    for (int g = 0; g < GROUPS; ++g) {
+        uint8_t* prow = pbuf + g * 128 * 128 + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < CHUNKS; ++ch) {
+            const float* pv = x + g * 64 + ch * 8;
+            uint4 pk;
+            pk.x = pack_bf16x2(pv[0], pv[1]);
+            pk.y = pack_bf16x2(pv[2], pv[3]);
+            pk.z = pack_bf16x2(pv[4], pv[5]);
+            pk.w = pack_bf16x2(pv[6], pv[7]);
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
+        }
+    }
+}
+
+// Epilogue: this thread's O row (NCOL fp32 columns in TMEM from t_col) times
+// `inv`, staged in shared memory in the TMA box layout and stored by TMA.
+//   bf16 output: boxes of 64 columns x 128 rows (128-byte rows, swizzled);
+//   fp32 partials: boxes of 32 columns x 128 rows.
+// Box b of the stage sits at stage + b * 16 KB.  All 128 threads of the four
+// softmax warps call this together; thread `leader` issues the stores (the
+// TMA store of commit e4ee9fd: bulk_group, commit_group, wait_group.read 0).
+// have_o must be uniform within each warp (tcgen05.ld is warp-collective);
+// if any thread set *abort_flag, nothing is stored.
+template <int NCOL, bool F32>
+__device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, int row, uint8_t* stage,
+                                                   const void* tmap, int col0, int row0_coord, int slab_coord,
+                                                   bool have_o, bool leader, const int* abort_flag) {
+#pragma unroll 1
+    for (int c = 0; c < NCOL / 32; ++c) {
+        float ov[32];
+        if (have_o) {
+            tmem_ld32(t_col + c * 32, ov);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
+        if constexpr (F32) {
+            uint8_t* rowp = stage + c * 16384 + row * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
+                                             ov[q * 4 + 3] * inv);
+                *reinterpret_cast<float4*>(rowp + ((q ^ (row & 7)) << 4)) = v;
+            }
+        } else {
+            uint8_t* rowp = stage + (c >> 1) * 16384 + row * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 pk;
+                pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                const int chunk = (c & 1) * 4 + q;
+                *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) = pk;
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(2, 128);
+    if (leader && *abort_flag == 0) {
+        constexpr int BOX_COLS = F32 ? 32 : 64;
+#pragma unroll 1
+        for (int b = 0; b < NCOL / BOX_COLS; ++b)
+            tma_store_3d(tmap, col0 + b * BOX_COLS, row0_coord, slab_coord, stage + b * 16384);
+        tma_store_commit();
+        tma_store_wait_read();
+    }
+}
+
+}  // namespace fmha

@@ -33,6 +33,7 @@
 #include <climits>
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace fmha {
 namespace {
@@ -46,7 +47,9 @@ struct TCfg {
     static constexpr int NB = HD / 64;                 // 64-column (128-byte) boxes
     static constexpr int Q_BYTES = BM * HD * 2;
     static constexpr int KV_TILE = BN * HD * 2;        // one K or V tile
-    static constexpr int P_BYTES = BM * BN * 2;        // one P buffer (two are kept)
+    static constexpr int P_GROUPS = (BN + 63) / 64;    // 128-byte swizzled row groups of P
+    static constexpr int P_CHUNKS = (BN < 64 ? BN : 64) / 8;  // 16-byte chunks per row and group
+    static constexpr int P_BYTES = BM * 128 * P_GROUPS;  // one P buffer (two are kept)
     static constexpr int THREADS = 224;
     static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
     static constexpr int O_COL = 2 * BN;
@@ -60,6 +63,7 @@ struct TCfg {
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HD <= TMEM_COLS, "S double buffer + O must fit in TMEM");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert((KST + VST) * KV_TILE >= BM * HD * 4, "the epilogue stages fp32 O in the K/V stages");
 };
 
 struct TcArgs {
@@ -86,7 +90,7 @@ __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, i
 template <int HD>
 __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const TcArgs a) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const TcArgs a) {
     using C = TCfg<HD>;
     constexpr int BM = C::BM, BN = C::BN, KST = C::KST, VST = C::VST;
     extern __shared__ uint8_t smem_raw[];
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     uint64_t* p_ready = s_full + 2;    // [2] by P buffer
     uint64_t* o_done = p_ready + 2;    // [2] by P buffer: PV of a tile using that P buffer completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rt = blockIdx.x, split = blockIdx.y, slab = blockIdx.z;
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             mbar_init(&p_ready[b2], 128);
             mbar_init(&o_done[b2], 1);
         }
+        *abort_flag = 0;
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -278,30 +284,9 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
             }
             tmem_wait_ld();
-            const int key0 = k_lo + j * BN;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                const int key = key0 + i;
-                x[i] = (key >= jlo && key <= jhi) ? x[i] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[i]);
-            }
-            float alpha = 1.f;
-            float m_new = m_ref;
-            if (mt > m_ref + 8.f) {
-                m_new = mt;
-                alpha = exp2f(m_ref - m_new);  // 0 when m_ref = -inf
-            }
-            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
             // Exponentials and the row sum before waiting on the tensor core.
-            float rs = 0.f;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                x[i] = exp2f(x[i] - mu);
-                rs += x[i];
-            }
-            l = l * alpha + rs;
-            m_ref = m_new;
+            float alpha;
+            softmax_row_tile<BN>(x, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, alpha);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
             // P buffer pb was last read by PV_{j-2}; a rescale of O needs PV_{j-1} done.
             if (rescale) {
@@ -315,20 +300,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                     break;
                 }
             }
-#pragma unroll
-            for (int g = 0; g < BN / 64; ++g) {
-                uint8_t* prow = sp + pb * C::P_BYTES + g * BM * 128 + row * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const float* pv = x + g * 64 + ch * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(pv[0], pv[1]);
-                    pk.y = pack_bf16x2(pv[2], pv[3]);
-                    pk.z = pack_bf16x2(pv[4], pv[5]);
-                    pk.w = pack_bf16x2(pv[6], pv[7]);
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
-                }
-            }
+            write_p_row<BN>(sp + pb * C::P_BYTES, row, x);
             if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
@@ -348,49 +320,28 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n_tiles > 0) ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
         constexpr float kLn2 = 0.693147180559945309f;
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        const long long gr = row0 + grow;
-        const long long prow = (long long)split * a.rows_total + gr;
-        if (ok) {
-#pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
-                float ov[32];
-                if (n_tiles > 0) {
-                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-                }
-                if (!valid) continue;
-                if (!a.to_partials) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + gr * HD + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
-                        pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
-                        pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
-                        pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
-                        dst[q] = pk;
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(a.o_part + prow * HD + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
-                                             ov[q * 4 + 3] * inv);
-                }
-            }
-            if (valid) {
-                if (!a.to_partials)
-                    a.lse[gr] = lse;
-                else
-                    a.lse_part[prow] = lse;
-            }
+        // O -> shared memory (the drained K/V stages) -> TMA store; rows past
+        // the slab's end fall outside the tensor map and are not written.
+        uint8_t* stage = sk;
+        if (!a.to_partials)
+            epilogue_tma_store<HD, false>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin, slab,
+                                          ok && n_tiles > 0, threadIdx.x == 64, abort_flag);
+        else
+            epilogue_tma_store<HD, true>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin,
+                                         split * (int)(a.rows_total / a.R) + slab, ok && n_tiles > 0,
+                                         threadIdx.x == 64, abort_flag);
+        if (valid && ok) {
+            const long long gr = row0 + grow;
+            if (!a.to_partials)
+                a.lse[gr] = lse;
+            else
+                a.lse_part[(long long)split * a.rows_total + gr] = lse;
         }
         tc_fence_before();
     }
@@ -434,13 +385,20 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     dim3 grid((L.p.R + C::BM - 1) / C::BM, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, a);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int tc_kv_tile(int hd) { return hd <= 128 ? 128 : 64; }
+int tc_kv_tile(int hd) {
+    switch (hd) {
+        case 64: return TCfg<64>::BN;
+        case 128: return TCfg<128>::BN;
+        case 256: return TCfg<256>::BN;
+        default: return 0;
+    }
+}
 
 bool tc_supports(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 

@@ -15,6 +15,7 @@
 #include <climits>
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace fmha {
 namespace {
@@ -39,6 +40,7 @@ struct WCfg {
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(NSLOT * SLOT_BYTES >= BM * HALF * 4, "the epilogue stages fp32 O in the ring");
 };
 
 struct WideArgs {
@@ -64,7 +66,8 @@ __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, in
 
 __global__ void __launch_bounds__(WCfg::THREADS, 1)
     fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const WideArgs a) {
+                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                       const WideArgs a) {
     using C = WCfg;
     constexpr int BM = C::BM, BN = C::BN;
     extern __shared__ uint8_t smem_raw[];
@@ -78,6 +81,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     uint64_t* p_ready = s_full + 2;
     uint64_t* o_done = p_ready + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rt = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -117,6 +121,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         mbar_init(&s_full[1], 1);
         mbar_init(p_ready, 128);
         mbar_init(o_done, 1);
+        *abort_flag = 0;
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -261,46 +266,14 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
             }
             tmem_wait_ld();
-            const int key0 = k_lo + j * BN;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                const int key = key0 + i;
-                x[i] = (key >= jlo && key <= jhi) ? x[i] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[i]);
-            }
-            float alpha = 1.f, m_new = m_ref;
-            if (mt > m_ref + 8.f) {
-                m_new = mt;
-                alpha = exp2f(m_ref - m_new);
-            }
-            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+            float alpha;
+            softmax_row_tile<BN>(x, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, alpha);
+            // PV_{j-1} must be complete before P is overwritten and O rescaled.
             if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
                 ok = false;
                 break;
             }
-            float rs = 0.f;
-#pragma unroll
-            for (int g = 0; g < BN / 64; ++g) {
-                uint8_t* prow = sp + g * BM * 128 + row * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        pv[e] = exp2f(x[g * 64 + ch * 8 + e] - mu);
-                        rs += pv[e];
-                    }
-                    uint4 pk;
-                    pk.x = pack_bf16x2(pv[0], pv[1]);
-                    pk.y = pack_bf16x2(pv[2], pv[3]);
-                    pk.z = pack_bf16x2(pv[4], pv[5]);
-                    pk.w = pack_bf16x2(pv[6], pv[7]);
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
-                }
-            }
-            l = l * alpha + rs;
-            m_ref = m_new;
+            write_p_row<BN>(sp, row, x);
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 tc_fence_after();
 #pragma unroll 1
@@ -319,50 +292,26 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             mbar_arrive(p_ready);
         }
         if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
         constexpr float kLn2 = 0.693147180559945309f;
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        const long long gr = row0 + grow;
-        const long long prow = (long long)split * a.rows_total + gr;
-        if (ok) {
-#pragma unroll 1
-            for (int c = 0; c < C::HALF / 32; ++c) {
-                float ov[32];
-                if (n_tiles > 0) {
-                    tmem_ld32(t_lane + C::O_COL + c * 32, ov);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-                }
-                if (!valid) continue;
-                const int col = half * C::HALF + c * 32;
-                if (!a.to_partials) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + gr * C::HD + col);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
-                        pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
-                        pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
-                        pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
-                        dst[q] = pk;
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(a.o_part + prow * C::HD + col);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
-                                             ov[q * 4 + 3] * inv);
-                }
-            }
-            if (valid && half == 0) {
-                if (!a.to_partials)
-                    a.lse[gr] = lse;
-                else
-                    a.lse_part[prow] = lse;
-            }
+        // This half of O -> shared memory (the drained ring) -> TMA store.
+        if (!a.to_partials)
+            epilogue_tma_store<C::HALF, false>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin, slab,
+                                               ok && n_tiles > 0, threadIdx.x == 64, abort_flag);
+        else
+            epilogue_tma_store<C::HALF, true>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+                                              split * (int)(a.rows_total / a.R) + slab, ok && n_tiles > 0,
+                                              threadIdx.x == 64, abort_flag);
+        if (valid && ok && half == 0) {
+            const long long gr = row0 + grow;
+            if (!a.to_partials)
+                a.lse[gr] = lse;
+            else
+                a.lse_part[(long long)split * a.rows_total + gr] = lse;
         }
         tc_fence_before();
     }
@@ -408,7 +357,7 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     dim3 grid(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
-    fwd_tc_wide_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, a);
+    fwd_tc_wide_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
     return cudaGetLastError();
 }
 
