@@ -107,8 +107,8 @@ def peaks():
 # only used while these files are unchanged.
 KERNEL_SOURCES = {
     "decode_splitkv": ("decode_kernel.cu", "ptx.cuh"),
-    "fwd_tc": ("tc_kernel.cu", "ptx.cuh"),
-    "fwd_tc_wide": ("tc_wide_kernel.cu", "ptx.cuh"),
+    "fwd_tc": ("tc_kernel.cu", "tc_common.cuh", "ptx.cuh"),
+    "fwd_tc_wide": ("tc_wide_kernel.cu", "tc_common.cuh", "ptx.cuh"),
     "merge_lse": ("merge_kernel.cu", "ptx.cuh"),
 }
 
@@ -343,8 +343,9 @@ def run_workload(binding, w, steps, warmup, stream, dist=None, sampler=None):
     binding.fmha_check_device_status(stream)
     ms = max_over_ranks(ms, dist)
     kern = measure_kernel_only(binding, w, sets, stream, steps)
+    single = kern["n_splits"] == 1
     res = {"ms_total": ms, "ms_per_step": ms / steps, "t0": t0, "t1": t1, "n_sets": len(sets), "l2_bytes": l2,
-           "launches_per_step": 1 if kern["n_splits"] == 1 else 2}
+           "launches_per_step": 1 if single else 2}
     res.update(kern)
     del sets
     torch.cuda.empty_cache()
