@@ -421,6 +421,29 @@ def roofline_obj(bytes_per_launch, ms, hbm_peak, peak_kind, traffic):
             "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "peak_source": peak_kind}
 
 
+def run_sweep():
+    """The MHA shape sweep (batch 4, 16 heads, hd x T x s_k, K x 3): GB/s and
+    TFLOP/s per point, one JSON line each."""
+    from head_attention_forward_fmha_gb300 import binding
+    binding.load()
+    hbm_peak, bf16_peak, _, peak_kind = peaks()
+    stream = torch.cuda.Stream()
+    for w in inputs.sweep():
+        b, f = algo_bytes(w), algo_flops(w)
+        est = b / (hbm_peak * 1e9)
+        steps = int(min(200, max(10, 2e-3 / max(est, 1e-7))))
+        r = run_workload(binding, w, steps, 3, stream)
+        sec = r["ms_per_step"] * 1e-3
+        print(json.dumps({
+            "workload": w.name, "hd": w.hd, "T": w.T, "s_k": w.s_k, "steps": steps,
+            "us_per_step": round(r["ms_per_step"] * 1e3, 2), "GB/s": round(b / sec / 1e9, 1),
+            "TFLOP/s": round(f / sec / 1e12, 2), "frac_hbm": round(b / sec / 1e9 / hbm_peak, 4),
+            "frac_bf16_peak": round(f / sec / 1e12 / bf16_peak, 4),
+            "frac_attainable": round(max(b / (hbm_peak * 1e9), f / (bf16_peak * 1e12)) / sec, 4),
+            "kernel": r["kernel"], "n_splits": r["n_splits"], "peak_source": peak_kind}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,7 +454,11 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every point of the MHA shape sweep, one JSON line per point (not the bench line)")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep()
     w = inputs.WORKLOADS[args.workload]
     hbm_peak, bf16_peak, bf16_sustained, peak_kind = peaks()
     bytes_step = algo_bytes(w)

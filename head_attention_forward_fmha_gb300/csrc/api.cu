@@ -142,9 +142,11 @@ int sm_count() {
 
 // ---------------------------------------------------------------- planning
 // Kernel families: the decode kernel (8 or 16 query rows per thread block,
-// mma.sync) and the tensor-core kernel (128 query rows, tcgen05).  A KV head
-// with at least kTcMinRows query rows goes to the tensor-core kernel.
-constexpr int kTcMinRows = 64;
+// mma.sync) and the tensor-core kernels (128 query rows, tcgen05).  A KV head
+// with at least tc_min_rows(hd) query rows goes to the tensor-core kernels:
+// 64 rows at hd <= 128, 32 rows at hd 256 and 512, where the decode kernel's
+// CUDA-core-side work per key grows with hd (measured on the MHA shape sweep).
+int tc_min_rows(int hd) { return hd >= 256 ? 32 : 64; }
 std::atomic<int> g_path_override{0};  // 0 auto, 1 decode kernel, 2 tensor-core kernel
 
 enum class Path { Decode, TensorCore, TensorCoreWide };
@@ -153,7 +155,7 @@ Path choose_path(const Problem& p) {
     const int ov = g_path_override.load();
     const bool tc_ok = tc_supports(p.hd) || p.hd == 512;
     if (ov == 1 || !tc_ok) return Path::Decode;
-    if (ov == 2 || p.R >= kTcMinRows) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
+    if (ov == 2 || p.R >= tc_min_rows(p.hd)) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
     return Path::Decode;
 }
 

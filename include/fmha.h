@@ -171,8 +171,8 @@ int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream);
 /*
  * Kernel-family selection for every later call in the process: 0 = automatic
  * (default: the 128-row tensor-core kernels when a KV head has at least 64
- * query rows, else the decode kernel), 1 = always the decode kernel, 2 =
- * always the tensor-core kernels.  Meant for tests and
+ * query rows at hd <= 128, or 32 at hd 256 and 512, else the decode kernel),
+ * 1 = always the decode kernel, 2 = always the tensor-core kernels.  Meant for tests and
  * measurements that compare the two families on one shape; results agree
  * within the documented tolerance.  Returns FMHA_ERR_SHAPE for other values.
  */
