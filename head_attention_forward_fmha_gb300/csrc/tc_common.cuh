@@ -93,54 +93,58 @@ __device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float 
 // Box b of the stage sits at stage + b * 16 KB.  All 128 threads of the four
 // softmax warps call this together; thread `leader` issues the stores (the
 // TMA store of commit e4ee9fd: bulk_group, commit_group, wait_group.read 0).
+// Boxes are stored as soon as they are staged, so the TMA reads box b while
+// the threads stage box b + 1; only the last read is waited for.
 // have_o must be uniform within each warp (tcgen05.ld is warp-collective);
 // if any thread set *abort_flag, nothing is stored.
 template <int NCOL, bool F32>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, int row, uint8_t* stage,
                                                    const void* tmap, int col0, int row0_coord, int slab_coord,
                                                    bool have_o, bool leader, const int* abort_flag) {
+    constexpr int BOX_COLS = F32 ? 32 : 64;
+    constexpr int CHUNKS_PER_BOX = BOX_COLS / 32;
 #pragma unroll 1
-    for (int c = 0; c < NCOL / 32; ++c) {
-        float ov[32];
-        if (have_o) {
-            tmem_ld32(t_col + c * 32, ov);
-            tmem_wait_ld();
-        } else {
+    for (int bx = 0; bx < NCOL / BOX_COLS; ++bx) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        for (int cc = 0; cc < CHUNKS_PER_BOX; ++cc) {
+            const int c = bx * CHUNKS_PER_BOX + cc;
+            float ov[32];
+            if (have_o) {
+                tmem_ld32(t_col + c * 32, ov);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+            }
+            uint8_t* rowp = stage + bx * 16384 + row * 128;
+            if constexpr (F32) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
+                                                 ov[q * 4 + 3] * inv);
+                    *reinterpret_cast<float4*>(rowp + ((q ^ (row & 7)) << 4)) = v;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                    pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                    pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                    pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                    const int chunk = cc * 4 + q;
+                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) = pk;
+                }
+            }
         }
-        if constexpr (F32) {
-            uint8_t* rowp = stage + c * 16384 + row * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv,
-                                             ov[q * 4 + 3] * inv);
-                *reinterpret_cast<float4*>(rowp + ((q ^ (row & 7)) << 4)) = v;
-            }
-        } else {
-            uint8_t* rowp = stage + (c >> 1) * 16384 + row * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 pk;
-                pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
-                pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
-                pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
-                pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
-                const int chunk = (c & 1) * 4 + q;
-                *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) = pk;
-            }
+        fence_proxy_async_smem();
+        named_barrier_sync(2, 128);
+        if (leader && *abort_flag == 0) {
+            tma_store_3d(tmap, col0 + bx * BOX_COLS, row0_coord, slab_coord, stage + bx * 16384);
+            tma_store_commit();
         }
     }
-    fence_proxy_async_smem();
-    named_barrier_sync(2, 128);
-    if (leader && *abort_flag == 0) {
-        constexpr int BOX_COLS = F32 ? 32 : 64;
-#pragma unroll 1
-        for (int b = 0; b < NCOL / BOX_COLS; ++b)
-            tma_store_3d(tmap, col0 + b * BOX_COLS, row0_coord, slab_coord, stage + b * 16384);
-        tma_store_commit();
-        tma_store_wait_read();
-    }
+    if (leader) tma_store_wait_read();
 }
 
 }  // namespace fmha
