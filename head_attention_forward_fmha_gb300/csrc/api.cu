@@ -329,7 +329,7 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
         rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
         if (rc) return rc;
-        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream);
+        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream, true);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {

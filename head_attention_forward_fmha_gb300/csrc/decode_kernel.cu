@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                           const DecodeArgs a) {
     using C = DCfg<HD, NB>;
+    launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;

@@ -61,8 +61,10 @@ int tc_wide_kv_tile();
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
 
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
+// dependent: launch as a programmatic dependent of the kernel just queued on
+// `stream` (that kernel must be one of this library's split kernels).
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows,
-                         int hd, void* o, float* lse, cudaStream_t stream);
+                         int hd, void* o, float* lse, cudaStream_t stream, bool dependent = false);
 
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).

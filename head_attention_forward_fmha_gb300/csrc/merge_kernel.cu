@@ -7,7 +7,9 @@
 // One warp per (output row, slice of up to 128 columns): the lanes first
 // share the chunk weights (lane i holds chunk i's weight), then stream the
 // slice of every partial with coalesced 8- or 16-byte loads, several chunks
-// in flight, and write one bf16 slice.
+// in flight, and write one bf16 slice.  Behind the split kernel, fmha_fwd
+// launches it as a programmatic dependent: its blocks are scheduled while the
+// split kernel runs and wait in grid_dependency_wait for the partials.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -38,6 +40,7 @@ template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n_splits,
                      long long rows, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
     using C = MCfg<HD>;
     constexpr int V = C::VEC;
     const int lane = threadIdx.x & 31;
@@ -106,24 +109,33 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 template <int HD>
 cudaError_t launch_t(const float* o_parts, const float* lse_parts, int n_splits, long long rows, void* o,
-                     float* lse, cudaStream_t stream) {
+                     float* lse, bool dependent, cudaStream_t stream) {
     const long long tasks = rows * MCfg<HD>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
-    merge_lse_kernel<HD><<<(unsigned)blocks, kMergeWarps * 32, 0, stream>>>(
-        o_parts, lse_parts, n_splits, rows, static_cast<__nv_bfloat16*>(o), lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD>, o_parts, lse_parts, n_splits, rows,
+                              static_cast<__nv_bfloat16*>(o), lse);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows, int hd,
-                         void* o, float* lse, cudaStream_t stream) {
+                         void* o, float* lse, cudaStream_t stream, bool dependent) {
     if (rows <= 0) return cudaSuccess;
     switch (hd) {
-        case 64: return launch_t<64>(o_parts, lse_parts, n_splits, rows, o, lse, stream);
-        case 128: return launch_t<128>(o_parts, lse_parts, n_splits, rows, o, lse, stream);
-        case 256: return launch_t<256>(o_parts, lse_parts, n_splits, rows, o, lse, stream);
-        case 512: return launch_t<512>(o_parts, lse_parts, n_splits, rows, o, lse, stream);
+        case 64: return launch_t<64>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
+        case 128: return launch_t<128>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
+        case 256: return launch_t<256>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
+        case 512: return launch_t<512>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -182,6 +182,13 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets a grid queued behind
+// this one with the programmatic-serialization attribute start early; that
+// grid's grid_dependency_wait returns once this grid has completed and its
+// memory is visible.  Both are no-ops when no such pairing exists.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace fmha
 
 // ---------------------------------------------------------------------------

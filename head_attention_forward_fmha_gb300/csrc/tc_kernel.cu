@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const TcArgs a) {
     using C = TCfg<HD>;
     constexpr int BM = C::BM, BN = C::BN, KST = C::KST, VST = C::VST;
+    launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sq = smem + C::OFF_Q;

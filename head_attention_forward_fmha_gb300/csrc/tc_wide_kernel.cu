@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                        const WideArgs a) {
     using C = WCfg;
     constexpr int BM = C::BM, BN = C::BN;
+    launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem + C::OFF_RING;
