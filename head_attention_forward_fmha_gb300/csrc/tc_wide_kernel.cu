@@ -29,6 +29,11 @@ struct WCfg {
     static constexpr int NSLOT = 8;
     static constexpr int QK_ITEMS = 2 * (HD / 64);     // Q chunk + K chunk per column block
     static constexpr int V_ITEMS = HALF / 64;
+    static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
+    // The V items of a tile start at a multiple of V_ITEMS and never wrap the
+    // ring, so they sit in V_ITEMS consecutive slots: PV is one N = 256 MMA
+    // per 16 keys over those slots.
+    static_assert(QK_ITEMS % V_ITEMS == 0 && NSLOT % V_ITEMS == 0, "V slots must be contiguous");
     static constexpr int P_BYTES = BM * BN * 2;
     static constexpr int THREADS = 192;
     static constexpr int O_COL = 2 * BN;
@@ -113,6 +118,45 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     const int k_lo = max(c_lo, u_lo), k_hi = min(c_hi, u_hi + 1);
     const int n_tiles = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
 
+    // Producer item sequence: QK(0), then for each tile j: QK(j+1) (if any)
+    // and V(j) -- the order the MMA warp consumes them in.  Item i -> kind
+    // (0 Q chunk, 1 K chunk, 2 V chunk), tile and 64-column chunk.
+    const int n_items = n_tiles * C::TILE_ITEMS;
+    auto item_of = [&](int i, int& kind, int& tile, int& c) {
+        if (i < C::QK_ITEMS) {
+            tile = 0;
+            kind = i & 1;
+            c = i >> 1;
+            return;
+        }
+        const int r = i - C::QK_ITEMS;
+        const int j = r / C::TILE_ITEMS, o = r - j * C::TILE_ITEMS;
+        if (j < n_tiles - 1 && o < C::QK_ITEMS) {
+            tile = j + 1;
+            kind = o & 1;
+            c = o >> 1;
+        } else {
+            tile = j;
+            kind = 2;
+            c = (j < n_tiles - 1) ? o - C::QK_ITEMS : o;
+        }
+    };
+    uint64_t pol_kv = 0, pol_q = 0;
+    auto issue_item = [&](int i) {
+        int kind, tile, c;
+        item_of(i, kind, tile, c);
+        const int s = i % C::NSLOT;
+        const int key = k_lo + tile * BN;
+        mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
+        uint8_t* dst = ring + s * C::SLOT_BYTES;
+        if (kind == 0)
+            tma_load_3d_hint(dst, &tmq, c * 64, r_begin, slab, &slot_full[s], pol_q);
+        else if (kind == 1)
+            tma_load_3d_hint(dst, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
+        else
+            tma_load_3d_hint(dst, &tmv, half * C::HALF + c * 64, key, slab, &slot_full[s], pol_kv);
+    };
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NSLOT; ++s) {
             mbar_init(&slot_full[s], 1);
@@ -124,6 +168,16 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         mbar_init(o_done, 1);
         *abort_flag = 0;
         mbar_fence_init();
+        // The first ring-full needs no free slot: start it before the block
+        // barrier and the TMEM allocation.
+        if (n_tiles > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            pol_kv = l2_policy_evict_first();
+            pol_q = l2_policy_evict_last();
+            for (int i = 0; i < min(C::NSLOT, n_items); ++i) issue_item(i);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -136,58 +190,19 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Item order: QK(0), then for each tile j: QK(j+1), V(j) -- the order
-        // the MMA warp consumes them in.
-        if (lane == 0 && n_tiles > 0) {
-            tma_prefetch_desc(&tmq);
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
-            const uint64_t pol_kv = l2_policy_evict_first();
-            const uint64_t pol_q = l2_policy_evict_last();
-            int item = 0;
-            bool ok = true;
-            auto slot_acquire = [&](int& s) -> bool {
-                s = item % C::NSLOT;
-                if (item >= C::NSLOT && !mbar_wait(&slot_empty[s], ((item / C::NSLOT) - 1) & 1, a.status))
-                    return false;
-                ++item;
-                return true;
-            };
-            auto load_qk = [&](int j) -> bool {
-                const int key = k_lo + j * BN;
-                for (int c = 0; c < C::HD / 64; ++c) {
-                    int s;
-                    if (!slot_acquire(s)) return false;
-                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
-                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, &slot_full[s], pol_q);
-                    if (!slot_acquire(s)) return false;
-                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
-                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
-                }
-                return true;
-            };
-            auto load_v = [&](int j) -> bool {
-                const int key = k_lo + j * BN;
-                for (int c = 0; c < C::V_ITEMS; ++c) {
-                    int s;
-                    if (!slot_acquire(s)) return false;
-                    mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
-                    tma_load_3d_hint(ring + s * C::SLOT_BYTES, &tmv, half * C::HALF + c * 64, key, slab,
-                                     &slot_full[s], pol_kv);
-                }
-                return true;
-            };
-            ok = load_qk(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles) ok = load_qk(j + 1);
-                if (ok) ok = load_v(j);
+        // Items 0 .. NSLOT-1 went out before the block barrier.
+        if (lane == 0) {
+            for (int i = C::NSLOT; i < n_items; ++i) {
+                const int s = i % C::NSLOT;
+                if (!mbar_wait(&slot_empty[s], ((i / C::NSLOT) - 1) & 1, a.status)) break;
+                issue_item(i);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, 64, 1);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, C::HALF, 1);
             const uint32_t ring_addr = smem_u32(ring), p_addr = smem_u32(sp);
             int item = 0;
             bool ok = true;
@@ -220,21 +235,25 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
                 if (!(ok = mbar_wait(p_ready, j & 1, a.status))) break;
                 tc_fence_after();
+                int sv0 = 0;
                 for (int c = 0; c < C::V_ITEMS && ok; ++c) {
                     int sv;
-                    if (!(ok = slot_take(sv))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t ad =
-                            smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(ring_addr + sv * C::SLOT_BYTES + kk * 16 * 128,
-                                                            BN * 128, 1024);
-                        tc_mma_f16(tmem + C::O_COL + c * 64, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&slot_empty[sv]);
+                    ok = slot_take(sv);
+                    if (c == 0) sv0 = sv;
                 }
-                if (ok) tc_commit(o_done);
+                if (!ok) break;
+                tc_fence_after();
+                // B: the V_ITEMS 64-column boxes of this half, one slot apart
+                // (the descriptor's leading byte offset); 16 keys per MMA.
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd =
+                        smem_desc_sw128(ring_addr + sv0 * C::SLOT_BYTES + kk * 16 * 128, C::SLOT_BYTES, 1024);
+                    tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                for (int c = 0; c < C::V_ITEMS; ++c) tc_commit(&slot_empty[sv0 + c]);
+                tc_commit(o_done);
             }
         }
     } else {
