@@ -231,20 +231,48 @@ int workspace(cudaStream_t stream, size_t bytes, void** out) {
     return FMHA_OK;
 }
 
-size_t partial_bytes(long long rows, int hd, int n_splits) {
-    return (size_t)n_splits * (size_t)rows * ((size_t)hd + 1) * sizeof(float);
+// Partial O (fp32, or fp16 plus two fp32 range factors per row) and fp32
+// partial LSE for n_splits chunks.
+size_t partial_bytes(long long rows, int hd, int n_splits, bool f16 = false) {
+    return (size_t)n_splits * (size_t)rows * ((size_t)hd * (f16 ? 2 : 4) + sizeof(float) * (f16 ? 3 : 1));
 }
 
-// A row-tile tensor [slabs, R, hd] (Q, O, or fp32 partials) viewed as 3-D;
+// fmha_fwd keeps hd-512 partials of the tensor-core kernel in fp16 (with a
+// power-of-two range factor per row half): there the partials are a large
+// share of the traffic, and fp16's 11 significant bits keep the merged error
+// well under the bf16 output's rounding.
+bool use_f16_partials(const Problem& p) { return p.hd == 512 && choose_path(p) == Path::TensorCoreWide; }
+
+// Workspace carve-up: o_part | lse_part [n, rows] | range_part [n, rows, 2] (fp16 only).
+struct PartialViews {
+    void* o_part;
+    float* lse_part;
+    float* range_part;
+};
+PartialViews partial_views(void* ws, long long rows, int hd, int n_splits, bool f16) {
+    PartialViews v;
+    v.o_part = ws;
+    v.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)n_splits * rows * hd * (f16 ? 2 : 4));
+    v.range_part = f16 ? v.lse_part + (size_t)n_splits * rows : nullptr;
+    return v;
+}
+
+enum RowsType { kRowsBf16, kRowsF32, kRowsF16 };
+
+// A row-tile tensor [slabs, R, hd] (Q, O, or partials) viewed as 3-D;
 // boxes of 128 bytes of columns x kTcRows rows, 128-byte swizzle.
-int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs, bool f32, const char* what) {
+int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs, RowsType type,
+                  const char* what) {
     if (!tensor_map_encoder()) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
-    const int esz = f32 ? 4 : 2;
+    const int esz = type == kRowsF32 ? 4 : 2;
+    const CUtensorMapDataType dt = type == kRowsF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : type == kRowsF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)R, (cuuint64_t)slabs};
     cuuint64_t strides[2] = {(cuuint64_t)hd * esz, (cuuint64_t)R * hd * esz};
     cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kTcRows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    CUresult r = g_encode(m, dt, 3,
                           const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -253,8 +281,11 @@ int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long sla
 }
 
 // Launch the kernel family the plan picks: O/LSE directly, or partials.
+// o_part is fp32, or fp16 with range_part when f16_parts (hd-512 tensor-core
+// kernel only).
 int run_kernel(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
-               float* lse, float* o_part, float* lse_part, bool to_partials, cudaStream_t stream) {
+               float* lse, void* o_part, float* lse_part, bool to_partials, cudaStream_t stream,
+               bool f16_parts = false, float* range_part = nullptr) {
     unsigned* status = device_status_word();
     if (!status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
     const Path path = choose_path(p);
@@ -266,14 +297,19 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.lse = lse;
         L.o_part = o_part;
         L.lse_part = lse_part;
+        L.range_part = range_part;
         L.to_partials = to_partials;
+        L.f16_partials = f16_parts;
+        if (f16_parts && (path != Path::TensorCoreWide || !range_part || !to_partials))
+            return fail(FMHA_ERR_LAUNCH, "fp16 partials need the hd-512 kernel and a range array");
         L.p = p;
         L.sp = sp;
         L.status = status;
-        int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, false, "Q");
+        int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, kRowsBf16, "Q");
         if (rc) return rc;
-        rc = to_partials ? make_rows_map(&L.tmap_o, o_part, p.hd, p.R, slabs * sp.n_splits, true, "O partials")
-                         : make_rows_map(&L.tmap_o, o, p.hd, p.R, slabs, false, "O");
+        rc = to_partials ? make_rows_map(&L.tmap_o, o_part, p.hd, p.R, slabs * sp.n_splits,
+                                         f16_parts ? kRowsF16 : kRowsF32, "O partials")
+                         : make_rows_map(&L.tmap_o, o, p.hd, p.R, slabs, kRowsBf16, "O");
         if (rc) return rc;
         rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, ks.kv_tile);
         if (rc) return rc;
@@ -283,11 +319,12 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
         return FMHA_OK;
     }
+    if (f16_parts) return fail(FMHA_ERR_LAUNCH, "fp16 partials need the hd-512 kernel");
     DecodeLaunch L;
     L.q = q;
     L.o = o;
     L.lse = lse;
-    L.o_part = o_part;
+    L.o_part = static_cast<float*>(o_part);
     L.lse_part = lse_part;
     L.to_partials = to_partials;
     L.p = p;
@@ -323,13 +360,14 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         if (sp.n_splits == 1)
             return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
         void* ws = nullptr;
-        rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits), &ws);
+        const bool f16 = use_f16_partials(p);
+        rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits, f16), &ws);
         if (rc) return rc;
-        float* o_part = static_cast<float*>(ws);
-        float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
-        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
+        const PartialViews pv = partial_views(ws, rows, hd, sp.n_splits, f16);
+        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, pv.o_part, pv.lse_part, true, stream, f16, pv.range_part);
         if (rc) return rc;
-        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream, true);
+        cudaError_t e =
+            launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream, true);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {
@@ -394,7 +432,7 @@ int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void*
     if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
         return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse buffers 4-byte aligned");
     if (rows > (1LL << 32)) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
-    cudaError_t e = launch_merge(o_parts, lse_parts, n_splits, rows, hd, o, lse, stream);
+    cudaError_t e = launch_merge(o_parts, lse_parts, nullptr, n_splits, rows, hd, false, o, lse, stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FMHA_OK;
 }
@@ -516,7 +554,7 @@ extern "C" int fmha_fwd_noalloc(const void* q, const void* k, const void* v, voi
         float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
         rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
         if (rc) return rc;
-        cudaError_t e = launch_merge(o_part, lse_part, sp.n_splits, rows, hd, o, lse, stream);
+        cudaError_t e = launch_merge(o_part, lse_part, nullptr, sp.n_splits, rows, hd, false, o, lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {

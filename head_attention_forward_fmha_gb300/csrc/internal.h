@@ -42,11 +42,15 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 struct TcLaunch {
     void* o;
     float* lse;
-    float* o_part;
+    void* o_part;       // fp32, or fp16 when f16_partials
     float* lse_part;
+    float* range_part;  // fp16 partials only: [n_splits, rows, 2] power-of-two factor per row half
     bool to_partials;
+    bool f16_partials;  // hd-512 kernel only
     CUtensorMap tmap_q, tmap_k, tmap_v;
-    CUtensorMap tmap_o;  // bf16 O [slabs, R, hd] (box 64 x 128), or fp32 partials [n_splits*slabs, R, hd] (box 32 x 128)
+    // bf16 O [slabs, R, hd] (box 64 x 128), fp32 partials [n_splits*slabs, R, hd]
+    // (box 32 x 128) or fp16 partials (box 64 x 128)
+    CUtensorMap tmap_o;
     Problem p;
     SplitPlan sp;
     unsigned* status;
@@ -63,8 +67,11 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
 // dependent: launch as a programmatic dependent of the kernel just queued on
 // `stream` (that kernel must be one of this library's split kernels).
-cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows,
-                         int hd, void* o, float* lse, cudaStream_t stream, bool dependent = false);
+// o_parts fp32, or fp16 (hd 512 only) with range_parts [n_splits, rows, 2]:
+// the stored fp16 value times range_parts[split, row, col / 256] is the partial.
+cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                         long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream,
+                         bool dependent = false);
 
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).

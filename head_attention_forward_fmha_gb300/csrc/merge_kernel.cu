@@ -7,7 +7,10 @@
 // One warp per (output row, slice of up to 128 columns): the lanes first
 // share the chunk weights (lane i holds chunk i's weight), then stream the
 // slice of every partial with coalesced 8- or 16-byte loads, several chunks
-// in flight, and write one bf16 slice.  Behind the split kernel, fmha_fwd
+// in flight, and write one bf16 slice.  Partials are fp32 (the public
+// layout) or fp16 (the workspace fmha_fwd uses at hd 512, where partials are a
+// large share of the traffic); an fp16 partial comes with a power-of-two range
+// factor per (chunk, row, 256-column half) that keeps it inside fp16's range.  Behind the split kernel, fmha_fwd
 // launches it as a programmatic dependent: its blocks are scheduled while the
 // split kernel runs and wait in grid_dependency_wait for the partials.
 #include "internal.h"
@@ -36,10 +39,25 @@ __device__ __forceinline__ void load_vec(const float* p, float (&v)[VEC]) {
     }
 }
 
-template <int HD>
+template <int VEC>
+__device__ __forceinline__ void load_vec(const __half* p, float (&v)[VEC]) {
+    if constexpr (VEC == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+        const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+        v[0] = a.x; v[1] = a.y;
+    }
+}
+
+template <int HD, typename PT>
 __global__ void __launch_bounds__(kMergeWarps * 32)
-    merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n_splits,
-                     long long rows, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    merge_lse_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                     const float* __restrict__ range_parts, int n_splits, long long rows,
+                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
     grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
     using C = MCfg<HD>;
     constexpr int V = C::VEC;
@@ -64,9 +82,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         for (int base = 0; base < n_splits; base += 32) {
             // lane i: weight of chunk base + i (0 for an empty chunk or past the end)
             const int mine = base + lane;
-            const float w_mine =
+            const float w_den =
                 (mine < n_splits) ? exp2f((__ldg(lse_parts + (long long)mine * rows + row) - mx) * kLog2e) : 0.f;
-            float wsum = w_mine;
+            float w_mine = w_den;  // weight of the stored values (times the range factor for fp16)
+            if constexpr (sizeof(PT) == 2) {
+                if (mine < n_splits) w_mine *= __ldg(range_parts + ((long long)mine * rows + row) * 2 + col / 256);
+            }
+            float wsum = w_den;
 #pragma unroll
             for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
             den += wsum;
@@ -107,9 +129,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     if (lane == 0 && col == 0) lse[row] = (den > 0.f) ? mx + log2f(den) * kLn2 : -INFINITY;
 }
 
-template <int HD>
-cudaError_t launch_t(const float* o_parts, const float* lse_parts, int n_splits, long long rows, void* o,
-                     float* lse, bool dependent, cudaStream_t stream) {
+template <int HD, typename PT>
+cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                     long long rows, void* o, float* lse, bool dependent, cudaStream_t stream) {
     const long long tasks = rows * MCfg<HD>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
@@ -122,20 +144,32 @@ cudaError_t launch_t(const float* o_parts, const float* lse_parts, int n_splits,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD>, o_parts, lse_parts, n_splits, rows,
+    return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT>, o_parts, lse_parts, range_parts, n_splits, rows,
                               static_cast<__nv_bfloat16*>(o), lse);
+}
+
+template <int HD>
+cudaError_t launch_hd(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                      long long rows, bool f16, void* o, float* lse, bool dependent, cudaStream_t stream) {
+    if (f16) {
+        if (HD != 512 || range_parts == nullptr) return cudaErrorInvalidValue;
+        return launch_t<HD>(static_cast<const __half*>(o_parts), lse_parts, range_parts, n_splits, rows, o, lse,
+                            dependent, stream);
+    }
+    return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse, dependent,
+                        stream);
 }
 
 }  // namespace
 
-cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_splits, long long rows, int hd,
-                         void* o, float* lse, cudaStream_t stream, bool dependent) {
+cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                         long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream, bool dependent) {
     if (rows <= 0) return cudaSuccess;
     switch (hd) {
-        case 64: return launch_t<64>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
-        case 128: return launch_t<128>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
-        case 256: return launch_t<256>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
-        case 512: return launch_t<512>(o_parts, lse_parts, n_splits, rows, o, lse, dependent, stream);
+        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
+        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
+        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
+        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -86,10 +86,17 @@ __device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float 
     }
 }
 
+// Output formats of the epilogue.
+enum OutMode : int {
+    kOutBf16 = 0,  // final O
+    kOutF32 = 1,   // split-KV partials, fp32 (the public partial layout)
+    kOutF16 = 2,   // split-KV partials, fp16 (fmha_fwd's workspace at hd 512)
+};
+
 // Epilogue: this thread's O row (NCOL fp32 columns in TMEM from t_col) times
 // `inv`, staged in shared memory in the TMA box layout and stored by TMA.
-//   bf16 output: boxes of 64 columns x 128 rows (128-byte rows, swizzled);
-//   fp32 partials: boxes of 32 columns x 128 rows.
+//   bf16 / fp16: boxes of 64 columns x 128 rows (128-byte rows, swizzled);
+//   fp32: boxes of 32 columns x 128 rows.
 // Box b of the stage sits at stage + b * 16 KB.  All 128 threads of the four
 // softmax warps call this together; thread `leader` issues the stores (the
 // TMA store of commit e4ee9fd: bulk_group, commit_group, wait_group.read 0).
@@ -97,10 +104,11 @@ __device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float 
 // the threads stage box b + 1; only the last read is waited for.
 // have_o must be uniform within each warp (tcgen05.ld is warp-collective);
 // if any thread set *abort_flag, nothing is stored.
-template <int NCOL, bool F32>
+template <int NCOL, int MODE>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, int row, uint8_t* stage,
                                                    const void* tmap, int col0, int row0_coord, int slab_coord,
                                                    bool have_o, bool leader, const int* abort_flag) {
+    constexpr bool F32 = MODE == kOutF32;
     constexpr int BOX_COLS = F32 ? 32 : 64;
     constexpr int CHUNKS_PER_BOX = BOX_COLS / 32;
 #pragma unroll 1
@@ -128,10 +136,17 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, in
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint4 pk;
-                    pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
-                    pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
-                    pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
-                    pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                    if constexpr (MODE == kOutF16) {
+                        pk.x = pack_f16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                        pk.y = pack_f16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                        pk.z = pack_f16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                        pk.w = pack_f16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                    } else {
+                        pk.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+                        pk.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+                        pk.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+                        pk.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+                    }
                     const int chunk = cc * 4 + q;
                     *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) = pk;
                 }

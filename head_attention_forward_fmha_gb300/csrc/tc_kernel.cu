@@ -331,10 +331,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         // the slab's end fall outside the tensor map and are not written.
         uint8_t* stage = sk;
         if (!a.to_partials)
-            epilogue_tma_store<HD, false>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin, slab,
+            epilogue_tma_store<HD, kOutBf16>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin, slab,
                                           ok && n_tiles > 0, threadIdx.x == 64, abort_flag);
         else
-            epilogue_tma_store<HD, true>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin,
+            epilogue_tma_store<HD, kOutF32>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin,
                                          split * (int)(a.rows_total / a.R) + slab, ok && n_tiles > 0,
                                          threadIdx.x == 64, abort_flag);
         if (valid && ok) {
@@ -369,7 +369,7 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     TcArgs a;
     a.o = static_cast<__nv_bfloat16*>(L.o);
     a.lse = L.lse;
-    a.o_part = L.o_part;
+    a.o_part = static_cast<float*>(L.o_part);
     a.lse_part = L.lse_part;
     a.to_partials = L.to_partials ? 1 : 0;
     a.n_h = L.p.n_h;

@@ -51,9 +51,10 @@ struct WCfg {
 struct WideArgs {
     __nv_bfloat16* o;
     float* lse;
-    float* o_part;
     float* lse_part;
+    float* range_part;  // fp16 partials: the power-of-two factor of each (split, row, half)
     int to_partials;
+    int part_f16;       // partials as fp16 (fmha_fwd's workspace) instead of fp32
     int n_h, n_kv_h, T, s_k, group, R, window, causal;
     float scale_log2;
     int kv_begin, kv_chunk;
@@ -316,16 +317,50 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
         constexpr float kLn2 = 0.693147180559945309f;
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        float inv = (l > 0.f) ? 1.f / l : 0.f;
         const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        const bool have_o = ok && n_tiles > 0;
+        float range = 1.f;
+        if (a.to_partials && a.part_f16) {
+            // fp16 keeps 11 significant bits only between 2^-14 and 65504: store
+            // O * 2^-k with k = floor(log2 max|O|) - 14, so this half-row's
+            // largest |O| lands in [2^14, 2^15), and record 2^k.  inv <= 1
+            // (l >= 1: the key at the running max contributes 2^0), so with
+            // |k| <= 113 neither inv * 2^-k nor 2^k overflows.
+            float mx = 0.f;
+            if (have_o) {
+#pragma unroll 1
+                for (int c = 0; c < C::HALF / 32; c += 4) {  // four loads in flight per wait
+                    float o0[32], o1[32], o2[32], o3[32];
+                    tmem_ld32(t_lane + C::O_COL + c * 32, o0);
+                    tmem_ld32(t_lane + C::O_COL + (c + 1) * 32, o1);
+                    tmem_ld32(t_lane + C::O_COL + (c + 2) * 32, o2);
+                    tmem_ld32(t_lane + C::O_COL + (c + 3) * 32, o3);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(o0[i]), fabsf(o1[i])), fmaxf(fabsf(o2[i]), fabsf(o3[i]))));
+                }
+            }
+            mx *= inv;
+            const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;  // floor(log2 mx) for normal mx
+            if (mx > 0.f && e < 128) {  // leave zero, inf and NaN rows as they are
+                const int k = min(max(e - 14, -113), 113);
+                inv *= __uint_as_float((uint32_t)(127 - k) << 23);  // 2^-k
+                range = __uint_as_float((uint32_t)(127 + k) << 23);
+            }
+        }
         // This half of O -> shared memory (the drained ring) -> TMA store.
+        const int pslab = split * (int)(a.rows_total / a.R) + slab;
         if (!a.to_partials)
-            epilogue_tma_store<C::HALF, false>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin, slab,
-                                               ok && n_tiles > 0, threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+                                                  slab, have_o, threadIdx.x == 64, abort_flag);
+        else if (a.part_f16)
+            epilogue_tma_store<C::HALF, kOutF16>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+                                                 pslab, have_o, threadIdx.x == 64, abort_flag);
         else
-            epilogue_tma_store<C::HALF, true>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
-                                              split * (int)(a.rows_total / a.R) + slab, ok && n_tiles > 0,
-                                              threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<C::HALF, kOutF32>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+                                                 pslab, have_o, threadIdx.x == 64, abort_flag);
         if (valid && ok && half == 0) {
             const long long gr = row0 + grow;
             if (!a.to_partials)
@@ -333,6 +368,8 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             else
                 a.lse_part[(long long)split * a.rows_total + gr] = lse;
         }
+        if (valid && ok && a.to_partials && a.part_f16)
+            a.range_part[((long long)split * a.rows_total + row0 + grow) * 2 + half] = range;
         tc_fence_before();
     }
     __syncthreads();
@@ -360,9 +397,10 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
     WideArgs a;
     a.o = static_cast<__nv_bfloat16*>(L.o);
     a.lse = L.lse;
-    a.o_part = L.o_part;
     a.lse_part = L.lse_part;
+    a.range_part = L.range_part;
     a.to_partials = L.to_partials ? 1 : 0;
+    a.part_f16 = L.f16_partials ? 1 : 0;
     a.n_h = L.p.n_h;
     a.n_kv_h = L.p.n_kv_h;
     a.T = L.p.T;

@@ -86,9 +86,12 @@ enum fmha_status {
  * window: sliding-window length in keys, 0 = none.  causal: 0 or 1.
  *
  * The library chooses whether to split the KV range over several thread
- * blocks.  When it splits, the fp32 partials live in a workspace the library
+ * blocks.  When it splits, the partials live in a workspace the library
  * allocates on `stream` with cudaMallocAsync the first time a (device,
  * stream) pair needs more than it holds, and keeps until fmha_release().
+ * They are fp32, except on the hd-512 tensor-core kernel, where they are fp16
+ * scaled by a power of two per row half (so any finite value keeps 11
+ * significant bits), which halves their traffic.
  * Callers that must not allocate use fmha_fwd_splitkv + fmha_merge with their
  * own buffers.
  */

@@ -86,3 +86,24 @@ def test_causal_prefill_both_families_agree(path):
     assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-3
     o_ref, lse_ref = oracle_full(w, q, k, v)
     compare(outs[1][0], outs[1][1], o_ref, lse_ref, "causal_prefill tc")
+
+
+@pytest.mark.parametrize("v_scale_log2", [0, 17, -20, 100])
+def test_hd512_fp16_workspace_keeps_range(v_scale_log2):
+    """fmha_fwd holds hd-512 split partials in fp16 with a power-of-two factor
+    per row half; V scaled by 2^17 (beyond fp16's 65504) or 2^-20 (below its
+    normal range) must come out as the same result scaled exactly."""
+    w = W("hd512_split_range", 2, 128, 1, 1, 512, 512)
+    n, _, kern = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, with_kernel=True)
+    assert kern == "fwd_tc_wide" and n > 1, (n, kern)
+    (q, k, v), (qd, kd, _) = device_inputs(w, seed=12)
+    s = 2.0 ** v_scale_log2
+    vd = (v.double() * s).to(torch.bfloat16).cuda()  # exact: a power-of-two multiple
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    o_back = o.double() / s
+    label = "V x 2^%d" % v_scale_log2
+    compare(o_back, lse, o_ref, lse_ref, label)
+    cosine_per_head(o_back, o_ref, label)
