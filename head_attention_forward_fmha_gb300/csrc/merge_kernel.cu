@@ -21,10 +21,12 @@ namespace {
 
 constexpr int kMergeWarps = 8;
 
-template <int HD>
+// VEC columns per lane: 16-byte loads of fp16 partials at hd >= 256, else
+// 8- or 16-byte loads of fp32 partials.
+template <int HD, typename PT>
 struct MCfg {
-    static constexpr int VEC = (HD >= 128) ? 4 : 2;  // fp32 columns per lane
-    static constexpr int SLICE = 32 * VEC;            // columns per warp
+    static constexpr int VEC = (sizeof(PT) == 2 && HD >= 256) ? 8 : (HD >= 128) ? 4 : 2;
+    static constexpr int SLICE = 32 * VEC;  // columns per warp
     static constexpr int NSLICE = HD / SLICE;
 };
 
@@ -41,7 +43,16 @@ __device__ __forceinline__ void load_vec(const float* p, float (&v)[VEC]) {
 
 template <int VEC>
 __device__ __forceinline__ void load_vec(const __half* p, float (&v)[VEC]) {
-    if constexpr (VEC == 4) {
+    if constexpr (VEC == 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+            v[2 * q] = f.x;
+            v[2 * q + 1] = f.y;
+        }
+    } else if constexpr (VEC == 4) {
         const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
         const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
@@ -59,7 +70,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                      const float* __restrict__ range_parts, int n_splits, long long rows,
                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
     grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
-    using C = MCfg<HD>;
+    using C = MCfg<HD, PT>;
     constexpr int V = C::VEC;
     const int lane = threadIdx.x & 31;
     const long long task = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
@@ -118,7 +129,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
     __nv_bfloat16* dst = o + row * HD + col;
-    if constexpr (V == 4) {
+    if constexpr (V == 8) {
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4*>(dst) = pk;
+    } else if constexpr (V == 4) {
         uint2 pk;
         pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
         pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
@@ -132,7 +150,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 template <int HD, typename PT>
 cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
                      long long rows, void* o, float* lse, bool dependent, cudaStream_t stream) {
-    const long long tasks = rows * MCfg<HD>::NSLICE;
+    const long long tasks = rows * MCfg<HD, PT>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
