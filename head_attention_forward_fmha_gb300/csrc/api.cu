@@ -367,7 +367,7 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, pv.o_part, pv.lse_part, true, stream, f16, pv.range_part);
         if (rc) return rc;
         cudaError_t e =
-            launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream, true);
+            launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {

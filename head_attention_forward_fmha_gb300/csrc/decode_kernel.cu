@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         mbar_fence_init();
     }
     __syncthreads();
+    grid_dependency_wait();  // every global access below follows the preceding kernel
 
     // ------------------------------------------------------------ producer
     if (warp == C::NCW) {
@@ -393,8 +394,15 @@ cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     a.status = L.status;
     const int row_tiles = (L.p.R + C::RT - 1) / C::RT;
     dim3 grid(row_tiles, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_k, L.tmap_v, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, a);
 }
 
 }  // namespace

@@ -64,14 +64,21 @@ cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream);
 int tc_wide_kv_tile();
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
 
+// Launch attribute shared by every kernel here: programmatic stream
+// serialization, so a kernel may be scheduled while its predecessor on the
+// stream finishes; each kernel runs its set-up (barriers, tensor memory,
+// descriptor prefetch) and then executes griddepcontrol.wait before its first
+// global memory access, which restores the full dependency.
+inline cudaLaunchAttribute programmatic_launch_attr() {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
+}
+
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
-// dependent: launch as a programmatic dependent of the kernel just queued on
-// `stream` (that kernel must be one of this library's split kernels).
-// o_parts fp32, or fp16 (hd 512 only) with range_parts [n_splits, rows, 2]:
-// the stored fp16 value times range_parts[split, row, col / 256] is the partial.
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                         long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream,
-                         bool dependent = false);
+                         long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream);
 
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).

@@ -10,8 +10,8 @@
 // in flight, and write one bf16 slice.  Partials are fp32 (the public
 // layout) or fp16 (the workspace fmha_fwd uses at hd 512, where partials are a
 // large share of the traffic); an fp16 partial comes with a power-of-two range
-// factor per (chunk, row, 256-column half) that keeps it inside fp16's range.  Behind the split kernel, fmha_fwd
-// launches it as a programmatic dependent: its blocks are scheduled while the
+// factor per (chunk, row, 256-column half) that keeps it inside fp16's range.
+// Launched as a programmatic dependent: its blocks are scheduled while the
 // split kernel runs and wait in grid_dependency_wait for the partials.
 #include "internal.h"
 #include "ptx.cuh"
@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                      const float* __restrict__ range_parts, int n_splits, long long rows,
                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
     grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
+    launch_dependents();     // the next kernel on the stream may start its set-up
     using C = MCfg<HD, PT>;
     constexpr int V = C::VEC;
     const int lane = threadIdx.x & 31;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 template <int HD, typename PT>
 cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                     long long rows, void* o, float* lse, bool dependent, cudaStream_t stream) {
+                     long long rows, void* o, float* lse, cudaStream_t stream) {
     const long long tasks = rows * MCfg<HD, PT>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
@@ -157,37 +158,35 @@ cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* ran
     cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
-    cfg.numAttrs = dependent ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT>, o_parts, lse_parts, range_parts, n_splits, rows,
                               static_cast<__nv_bfloat16*>(o), lse);
 }
 
 template <int HD>
 cudaError_t launch_hd(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                      long long rows, bool f16, void* o, float* lse, bool dependent, cudaStream_t stream) {
+                      long long rows, bool f16, void* o, float* lse, cudaStream_t stream) {
     if (f16) {
         if (HD != 512 || range_parts == nullptr) return cudaErrorInvalidValue;
         return launch_t<HD>(static_cast<const __half*>(o_parts), lse_parts, range_parts, n_splits, rows, o, lse,
-                            dependent, stream);
+                            stream);
     }
-    return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse, dependent,
+    return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse,
                         stream);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                         long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream, bool dependent) {
+                         long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     switch (hd) {
-        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
-        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
-        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
-        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, dependent, stream);
+        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
+        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
+        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
+        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
         default: return cudaErrorInvalidValue;
     }
 }

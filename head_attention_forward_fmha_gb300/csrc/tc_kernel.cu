@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // every global access below follows the preceding kernel
 
     if (warp == 0) {
         // ------------------------------------------------------------ Q / K producer
@@ -386,8 +387,15 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     dim3 grid((L.p.R + C::BM - 1) / C::BM, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
 }
 
 }  // namespace

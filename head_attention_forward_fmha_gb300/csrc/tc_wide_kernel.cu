@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             tma_prefetch_desc(&tmv);
             pol_kv = l2_policy_evict_first();
             pol_q = l2_policy_evict_last();
+            grid_dependency_wait();  // the preceding kernel's writes (Q, K, V) are visible
             for (int i = 0; i < min(C::NSLOT, n_items); ++i) issue_item(i);
         }
     }
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // every global access below follows the preceding kernel
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -414,9 +416,15 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
     a.kv_chunk = L.sp.kv_chunk;
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
-    dim3 grid(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
-    fwd_tc_wide_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
 }
 
 }  // namespace fmha

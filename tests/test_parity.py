@@ -164,3 +164,38 @@ def test_sweep_full_size_sampled_rows(w):
     compare(og, lg, o_ref, lse_ref, w.name)
     del qd, kd, vd, o, lse
     torch.cuda.empty_cache()
+
+
+CHAIN = [
+    # each kernel family, split and unsplit; O of one call is Q of the next
+    W("chain_hd512_mqa_split", 2, 128, 1, 1, 512, 512),
+    W("chain_gqa_decode_split", 4, 16, 2, 1, 2000, 128),
+    W("chain_tc_prefill", 2, 4, 4, 128, 256, 256, causal=True),
+]
+
+
+@pytest.mark.parametrize("w", CHAIN, ids=[w.name for w in CHAIN])
+def test_back_to_back_calls_see_previous_output(w):
+    """Consecutive calls on one stream may overlap their set-up with the
+    previous kernel (programmatic launches); each must still read the complete
+    output of the call before it.  Four calls are queued with no host sync,
+    call i+1 taking call i's O as its Q, into buffers that first hold NaN."""
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=21)
+    n = 4
+    outs = [torch.full_like(qd, float("nan")) for _ in range(n)]
+    lses = [torch.full(qd.shape[:-1], float("nan"), dtype=torch.float32, device="cuda") for _ in range(n)]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        src = qd
+        for i in range(n):
+            binding.fmha_fwd(src, kd, vd, outs[i], lses[i], scale=w.scale, window=w.window, causal=w.causal,
+                             stream=stream)
+            src = outs[i]
+    stream.synchronize()
+    binding.fmha_check_device_status()
+    src = q
+    for i in range(n):
+        o_ref, lse_ref = oracle_full(w, src, k, v)
+        compare(outs[i], lses[i], o_ref, lse_ref, "%s call %d" % (w.name, i))
+        src = outs[i].cpu()
