@@ -299,20 +299,35 @@ def measure_kernel_only(binding, w, sets, stream, steps):
         out["decode_ms"] = graph_time(fwd, len(sets), steps, stream) / steps
         out["merge_ms"] = 0.0
         return out
+    # The same kernels in the same configuration as fmha_fwd: its hd-512
+    # tensor-core path keeps fp16 partials (FMHA_PARTS_F16), the others fp32.
+    f16 = kernel == "fwd_tc_wide"
+    out["parts_format"] = "f16" if f16 else "f32"
     parts = []
     for (q, k, v, o, lse) in sets:
-        op = torch.empty((n_splits, w.batch, w.n_h, w.T, w.hd), dtype=torch.float32, device="cuda")
+        op = torch.empty((n_splits, w.batch, w.n_h, w.T, w.hd), dtype=torch.float16 if f16 else torch.float32,
+                         device="cuda")
         lp = torch.empty((n_splits, w.batch, w.n_h, w.T), dtype=torch.float32, device="cuda")
-        parts.append((op, lp))
+        rp = torch.empty((n_splits, w.batch, w.n_h, w.T, 2), dtype=torch.float32, device="cuda") if f16 else None
+        parts.append((op, lp, rp))
 
     def split(i):
         q, k, v, o, lse = sets[i]
-        binding.fmha_fwd_splitkv(q, k, v, chunk, parts[i][0], parts[i][1], scale=w.scale, window=w.window,
-                                 causal=w.causal, stream=stream)
+        op, lp, rp = parts[i]
+        if f16:
+            binding.fmha_fwd_splitkv_f16(q, k, v, chunk, op, lp, rp, scale=w.scale, window=w.window,
+                                         causal=w.causal, stream=stream)
+        else:
+            binding.fmha_fwd_splitkv(q, k, v, chunk, op, lp, scale=w.scale, window=w.window, causal=w.causal,
+                                     stream=stream)
 
     def merge(i):
         q, k, v, o, lse = sets[i]
-        binding.fmha_merge(parts[i][0], parts[i][1], o, lse, stream=stream)
+        op, lp, rp = parts[i]
+        if f16:
+            binding.fmha_merge_f16(op, lp, rp, o, lse, stream=stream)
+        else:
+            binding.fmha_merge(op, lp, o, lse, stream=stream)
 
     split(0)
     merge(0)
@@ -538,7 +553,8 @@ def main():
                    "l2": "inputs rotated over %d copies (%.0f MB > 2x L2 %.0f MB)"
                          % (res["n_sets"], res["n_sets"] * bytes_step / 1e6, res["l2_bytes"] / 1e6),
                    "timing": "CUDA graphs of fmha_fwd calls, CUDA events on the launching stream",
-                   "n_splits": res["n_splits"], "kv_chunk": res["kv_chunk"]},
+                   "n_splits": res["n_splits"], "kv_chunk": res["kv_chunk"],
+                   "partials": res.get("parts_format", "none")},
         "roofline": dict(roofline_obj(bytes_step, res["decode_ms"], hbm_peak, peak_kind, traffic),
                          kernel=res["kernel"]),
         "kernels_ms": {res["kernel"]: round(res["decode_ms"], 6), "merge_lse": round(res["merge_ms"], 6)},

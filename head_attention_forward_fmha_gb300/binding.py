@@ -19,7 +19,10 @@ FMHA_OK = 0
 ERRORS = {
     -1: "FMHA_ERR_NULL", -2: "FMHA_ERR_ALIGN", -3: "FMHA_ERR_HEADDIM", -4: "FMHA_ERR_HEADS",
     -5: "FMHA_ERR_SHAPE", -6: "FMHA_ERR_WORKSPACE", -7: "FMHA_ERR_LAUNCH", -8: "FMHA_ERR_DEVICE_TIMEOUT",
+    -9: "FMHA_ERR_UNSUPPORTED",
 }
+# Partial formats (enum fmha_parts_format).
+PARTS_F32, PARTS_F16 = 0, 1
 
 # Every symbol include/fmha.h declares, with its ctypes signature.
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -31,6 +34,9 @@ SIGNATURES = {
     "fmha_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp],
                          _i32),
     "fmha_merge": ([_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "fmha_fwd_splitkv_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                             _i32, _vp], _i32),
+    "fmha_merge_ex": ([_vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "fmha_splitkv_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32], _sz),
     "fmha_check_device_status": ([_vp], _i32),
     "fmha_get_last_error": ([], ctypes.c_char_p),
@@ -176,6 +182,49 @@ def fmha_merge(o_parts, lse_parts, o=None, lse=None, stream=None):
     rc = load().fmha_merge(_f32(o_parts, "o_parts"), _f32(lse_parts, "lse_parts"), n, _bf16(o, "o"),
                            _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
     _check(rc, "fmha_merge")
+    return o, lse
+
+
+def fmha_fwd_splitkv_f16(q, k, v, kv_chunk, o_parts=None, lse_parts=None, range_parts=None, scale=None, window=0,
+                         causal=False, stream=None):
+    """fp16 partials (FMHA_PARTS_F16): O_i * 2^-k as fp16 [n,b,n_h,T,hd], lse_i fp32 [n,b,n_h,T] and the
+    factors 2^k fp32 [n,b,n_h,T,2] (one per 256-column half row).  hd-512 tensor-core kernel only."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    _, n = fmha_split_layout(T, s_k, window, kv_chunk)
+    if o_parts is None:
+        o_parts = torch.empty((n, b, n_h, T, hd), dtype=torch.float16, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((n, b, n_h, T), dtype=torch.float32, device=q.device)
+    if range_parts is None:
+        range_parts = torch.empty((n, b, n_h, T, 2), dtype=torch.float32, device=q.device)
+    if (o_parts.dtype != torch.float16 or not o_parts.is_cuda or not o_parts.is_contiguous()
+            or o_parts.numel() < n * b * n_h * T * hd or lse_parts.numel() < n * b * n_h * T
+            or range_parts.numel() < n * b * n_h * T * 2):
+        raise ValueError("fp16 partial buffers too small or of the wrong type for %d chunks" % n)
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd_splitkv_ex(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), o_parts.data_ptr(),
+                                    _f32(lse_parts, "lse_parts"), _f32(range_parts, "range_parts"), PARTS_F16,
+                                    int(kv_chunk), b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
+                                    int(bool(causal)), _stream(stream))
+    _check(rc, "fmha_fwd_splitkv_ex")
+    return o_parts, lse_parts, range_parts
+
+
+def fmha_merge_f16(o_parts, lse_parts, range_parts, o=None, lse=None, stream=None):
+    """Merge FMHA_PARTS_F16 partials into bf16 O and fp32 LSE."""
+    if o_parts.dim() != 5 or o_parts.dtype != torch.float16 or not o_parts.is_contiguous():
+        raise ValueError("o_parts: contiguous fp16 [n,b,n_h,T,hd] expected")
+    n, b, n_h, T, hd = o_parts.shape
+    if tuple(lse_parts.shape) != (n, b, n_h, T) or tuple(range_parts.shape) != (n, b, n_h, T, 2):
+        raise ValueError("lse_parts [n,b,n_h,T] and range_parts [n,b,n_h,T,2] expected")
+    if o is None:
+        o = torch.empty((b, n_h, T, hd), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((b, n_h, T), dtype=torch.float32, device=o_parts.device)
+    rc = load().fmha_merge_ex(o_parts.data_ptr(), _f32(lse_parts, "lse_parts"), _f32(range_parts, "range_parts"),
+                              PARTS_F16, n, _bf16(o, "o"), _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
+    _check(rc, "fmha_merge_ex")
     return o, lse
 
 

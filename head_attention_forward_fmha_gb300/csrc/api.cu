@@ -397,44 +397,71 @@ int fmha_split_layout(int T, int s_k, int window, int kv_chunk, int* first_key) 
     return sp.n_splits;
 }
 
-int fmha_fwd_splitkv(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts, int kv_chunk,
-                     int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
-                     fmha_stream_t stream) {
+int fmha_fwd_splitkv_ex(const void* q, const void* k, const void* v, void* o_parts, float* lse_parts,
+                        float* range_parts, int parts_format, int kv_chunk, int batch, int n_h, int n_kv_h, int T,
+                        int s_k, int hd, float scale, int window, int causal, fmha_stream_t stream) {
     try {
         Problem p;
         int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
         if (rc) return rc;
+        if (parts_format != FMHA_PARTS_F32 && parts_format != FMHA_PARTS_F16)
+            return fail(FMHA_ERR_SHAPE, "parts_format=%d is not a partial format", parts_format);
+        const bool f16 = parts_format == FMHA_PARTS_F16;
+        if (f16 && !use_f16_partials(p))
+            return fail(FMHA_ERR_UNSUPPORTED, "fp16 partials are written by the hd-512 tensor-core kernel only "
+                                              "(hd=%d, %d query rows per KV head)", hd, p.R);
         rc = check_inputs(q, k, v, s_k);
         if (rc) return rc;
         if (kv_chunk < 1) return fail(FMHA_ERR_SHAPE, "kv_chunk=%d must be >= 1", kv_chunk);
-        if (!o_parts || !lse_parts) return fail(FMHA_ERR_NULL, "o_parts and lse_parts must be non-NULL");
-        if (!aligned(o_parts, 16) || !aligned(lse_parts, 4))
-            return fail(FMHA_ERR_ALIGN, "o_parts must be 16-byte, lse_parts 4-byte aligned");
+        if (!o_parts || !lse_parts || (f16 && !range_parts))
+            return fail(FMHA_ERR_NULL, "o_parts, lse_parts (and range_parts for fp16) must be non-NULL");
+        if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || (f16 && !aligned(range_parts, 4)))
+            return fail(FMHA_ERR_ALIGN, "o_parts must be 16-byte, lse_parts and range_parts 4-byte aligned");
         const long long rows = (long long)batch * n_h * T;
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = split_layout(T, s_k, window, kv_chunk);
         if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks (%d)", sp.n_splits);
-        return run_kernel(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream);
+        return run_kernel(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream, f16,
+                          f16 ? range_parts : nullptr);
     } catch (...) {
         return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_splitkv");
     }
 }
 
-int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void* o, float* lse, int batch, int n_h,
-               int T, int hd, fmha_stream_t stream) {
+int fmha_fwd_splitkv(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts, int kv_chunk,
+                     int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                     fmha_stream_t stream) {
+    return fmha_fwd_splitkv_ex(q, k, v, o_parts, lse_parts, nullptr, FMHA_PARTS_F32, kv_chunk, batch, n_h, n_kv_h,
+                               T, s_k, hd, scale, window, causal, stream);
+}
+
+int fmha_merge_ex(const void* o_parts, const float* lse_parts, const float* range_parts, int parts_format,
+                  int n_splits, void* o, float* lse, int batch, int n_h, int T, int hd, fmha_stream_t stream) {
     if (hd != 64 && hd != 128 && hd != 256 && hd != 512)
         return fail(FMHA_ERR_HEADDIM, "hd=%d: supported head dims are 64, 128, 256, 512", hd);
     if (batch < 0 || n_h < 0 || T < 0 || n_splits < 1)
         return fail(FMHA_ERR_SHAPE, "fmha_merge: need batch, n_h, T >= 0 and n_splits >= 1");
+    if (parts_format != FMHA_PARTS_F32 && parts_format != FMHA_PARTS_F16)
+        return fail(FMHA_ERR_SHAPE, "parts_format=%d is not a partial format", parts_format);
+    const bool f16 = parts_format == FMHA_PARTS_F16;
+    if (f16 && hd != 512) return fail(FMHA_ERR_UNSUPPORTED, "fp16 partials exist for hd = 512 only");
     const long long rows = (long long)batch * n_h * T;
     if (rows == 0) return FMHA_OK;
-    if (!o_parts || !lse_parts || !o || !lse) return fail(FMHA_ERR_NULL, "fmha_merge: NULL buffer");
-    if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
-        return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse buffers 4-byte aligned");
+    if (!o_parts || !lse_parts || !o || !lse || (f16 && !range_parts))
+        return fail(FMHA_ERR_NULL, "fmha_merge: NULL buffer");
+    if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4) ||
+        (f16 && !aligned(range_parts, 4)))
+        return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse and range buffers 4-byte aligned");
     if (rows > (1LL << 32)) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
-    cudaError_t e = launch_merge(o_parts, lse_parts, nullptr, n_splits, rows, hd, false, o, lse, stream);
+    cudaError_t e = launch_merge(o_parts, lse_parts, f16 ? range_parts : nullptr, n_splits, rows, hd, f16, o, lse,
+                                 stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FMHA_OK;
+}
+
+int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void* o, float* lse, int batch, int n_h,
+               int T, int hd, fmha_stream_t stream) {
+    return fmha_merge_ex(o_parts, lse_parts, nullptr, FMHA_PARTS_F32, n_splits, o, lse, batch, n_h, T, hd, stream);
 }
 
 size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits) {

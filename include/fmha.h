@@ -76,7 +76,8 @@ enum fmha_status {
     FMHA_ERR_SHAPE = -5,          /* negative size, causal with T > s_k, grid limits, bad window/chunk/scale */
     FMHA_ERR_WORKSPACE = -6,      /* the internal split-KV workspace could not be allocated */
     FMHA_ERR_LAUNCH = -7,         /* a CUDA call failed; the message names it */
-    FMHA_ERR_DEVICE_TIMEOUT = -8  /* a kernel's bounded wait gave up (from fmha_check_device_status) */
+    FMHA_ERR_DEVICE_TIMEOUT = -8, /* a kernel's bounded wait gave up (from fmha_check_device_status) */
+    FMHA_ERR_UNSUPPORTED = -9     /* a partial format this shape's kernel does not write */
 };
 
 /*
@@ -142,6 +143,37 @@ int fmha_fwd_splitkv(const void* q, const void* k, const void* v,
 int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits,
                void* o, float* lse, int batch, int n_h, int T, int hd,
                fmha_stream_t stream);
+
+/*
+ * Partial formats for fmha_fwd_splitkv_ex / fmha_merge_ex.  The merge formula
+ * is the one above; only the storage of O_i differs.
+ *   FMHA_PARTS_F32: o_parts fp32 [n_splits, batch, n_h, T, hd] (what
+ *     fmha_fwd_splitkv writes); range_parts unused, may be NULL.
+ *   FMHA_PARTS_F16: o_parts fp16 [n_splits, batch, n_h, T, hd] holding
+ *     O_i * 2^-k, and range_parts fp32 [n_splits, batch, n_h, T, 2] holding
+ *     2^k for each 256-column half of each row; k is chosen per half row so
+ *     that its largest |O_i| lies in [2^14, 2^15), so every finite partial
+ *     keeps fp16's 11 significant bits and none overflows.  Half the bytes of
+ *     FMHA_PARTS_F32 (for callers that move partials elsewhere before merging;
+ *     fmha_fwd uses this format internally at hd 512).  Written only by the
+ *     hd-512 tensor-core kernel: hd = 512 and fmha_fwd_plan reporting kernel 3,
+ *     else FMHA_ERR_UNSUPPORTED.  range_parts must be 4-byte aligned.
+ * This extension has no counterpart on the pages; it is a storage format of
+ * the partials whose merge they define.
+ */
+enum fmha_parts_format { FMHA_PARTS_F32 = 0, FMHA_PARTS_F16 = 1 };
+
+/* fmha_fwd_splitkv writing partials in `parts_format`. */
+int fmha_fwd_splitkv_ex(const void* q, const void* k, const void* v,
+                        void* o_parts, float* lse_parts, float* range_parts, int parts_format,
+                        int kv_chunk, int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                        float scale, int window, int causal, fmha_stream_t stream);
+
+/* fmha_merge of partials in `parts_format` (range_parts as written by
+ * fmha_fwd_splitkv_ex; FMHA_PARTS_F16 needs hd = 512). */
+int fmha_merge_ex(const void* o_parts, const float* lse_parts, const float* range_parts, int parts_format,
+                  int n_splits, void* o, float* lse, int batch, int n_h, int T, int hd,
+                  fmha_stream_t stream);
 
 /* Bytes of fp32 partial output (o_parts + lse_parts) that fmha_fwd_splitkv
  * writes for n_splits chunks. */

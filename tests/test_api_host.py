@@ -109,6 +109,22 @@ def test_splitkv_and_merge_argument_errors(lib):
     assert lib.fmha_split_layout(1, 10, 0, 0, None) == -5
 
 
+def test_f16_partials_only_on_the_hd512_tensor_core_kernel(lib):
+    f = lib.fmha_fwd_splitkv_ex
+    # hd 128: the fp16 partial format does not exist there
+    assert f(16, 16, 16, 16, 16, 16, 1, 64, 1, 64, 1, 1, 100, 128, 0.1, 0, 0, None) == -9
+    # hd 512 with 8 query rows per KV head runs on the decode kernel: unsupported too
+    assert f(16, 16, 16, 16, 16, 16, 1, 64, 1, 8, 1, 1, 100, 512, 0.1, 0, 0, None) == -9
+    # hd 512 with 128 rows per KV head: accepted up to the pointer checks
+    assert f(16, 16, 16, 16, 16, 0, 1, 128, 1, 128, 1, 1, 256, 512, 0.1, 0, 0, None) == -1   # range NULL
+    assert f(16, 16, 16, 16, 16, 18, 1, 128, 1, 128, 1, 1, 256, 512, 0.1, 0, 0, None) == -2  # range misaligned
+    assert f(16, 16, 16, 16, 16, 16, 7, 128, 1, 128, 1, 1, 256, 512, 0.1, 0, 0, None) == -5  # no such format
+    m = lib.fmha_merge_ex
+    assert m(16, 16, 16, 1, 2, 16, 16, 1, 1, 1, 128, None) == -9
+    assert m(16, 16, 0, 1, 2, 16, 16, 1, 1, 1, 512, None) == -1
+    assert m(16, 16, 16, 1, 2, 16, 16, 0, 1, 1, 512, None) == 0                      # empty
+
+
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(ImportError):
         binding.load(str(tmp_path / "nope.so"))

@@ -107,3 +107,29 @@ def test_hd512_fp16_workspace_keeps_range(v_scale_log2):
     label = "V x 2^%d" % v_scale_log2
     compare(o_back, lse, o_ref, lse_ref, label)
     cosine_per_head(o_back, o_ref, label)
+
+
+@pytest.mark.parametrize("chunk", [128, 200])
+def test_f16_partial_format_matches_oracle_and_fmha_fwd(chunk):
+    """FMHA_PARTS_F16: the stored fp16 values times their range factors are the
+    oracle's partials, the merge of them is the oracle's merge, and with
+    fmha_fwd's own chunking the pair reproduces fmha_fwd bit for bit."""
+    w = W("hd512_f16_parts", 2, 128, 1, 1, 700, 512, window=500)
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=14)
+    op, lp, rp = binding.fmha_fwd_splitkv_f16(qd, kd, vd, chunk, scale=w.scale, window=w.window)
+    o, lse = binding.fmha_merge_f16(op, lp, rp)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    n, b, n_h, T, hd = op.shape
+    deq = op.double() * rp.double().repeat_interleave(hd // 2, dim=-1)
+    op_ref, lp_ref = oracle.partials(to_np_bits(q), to_np_bits(k), to_np_bits(v), w.scale, chunk, w.window, False)
+    compare(deq, lp, op_ref, lp_ref, "f16 partials chunk %d" % chunk)
+    o_ref, lse_ref = oracle.merge(op_ref, lp_ref)
+    compare(o, lse, o_ref, lse_ref, "f16 merged chunk %d" % chunk)
+    n_plan, chunk_plan = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal)
+    op2, lp2, rp2 = binding.fmha_fwd_splitkv_f16(qd, kd, vd, chunk_plan, scale=w.scale, window=w.window)
+    o2, lse2 = binding.fmha_merge_f16(op2, lp2, rp2)
+    o3, lse3 = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window)
+    torch.cuda.synchronize()
+    assert op2.shape[0] == n_plan
+    assert torch.equal(o2, o3) and torch.equal(lse2, lse3)
