@@ -401,7 +401,7 @@ def run_e2e(binding, w, steps, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline(w, budget_s=10.0):
+def cpu_baseline(w, budget_s=12.0):
     """The fp64 oracle on the host cores over a bounded sample of the workload."""
     import numpy as np
     import oracle
@@ -413,7 +413,7 @@ def cpu_baseline(w, budget_s=10.0):
     t = time.time()
     oracle.attention_rows(qb, kb, vb, probe, w.scale, w.window, w.causal)
     per_row = max(1e-7, (time.time() - t) / len(probe))
-    n_rows = int(max(1, min(total_rows * 50, budget_s / per_row)))
+    n_rows = int(max(1, min(total_rows * 2000, budget_s / per_row)))
     done = 0
     t = time.time()
     while done < n_rows:
@@ -468,7 +468,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the MHA shape sweep, one JSON line per point (not the bench line)")
     args = ap.parse_args()
