@@ -8,7 +8,9 @@ What it computes is the plain definition of softmax attention (see
 ``fmha_oracle.c`` for the page citations and the readings taken):
 ``O = softmax(scale * Q K^T + mask) V`` per (batch, head, query row), in double
 precision, with the natural-log LSE of the scaled, masked logits, and the
-split-KV merge ``O = sum_i exp(lse_i) O_i / sum_i exp(lse_i)``.
+split-KV merge ``O = sum_i exp(lse_i) O_i / sum_i exp(lse_i)``.  An optional
+per-head attention-sink logit joins the softmax denominator only (the reading
+``fmha_oracle.c`` states for the pages' undefined "D5c sink").
 
 Inputs are numpy arrays: ``float64``, or ``uint16`` holding bf16 bit patterns
 (widened exactly inside the C code).  Shapes: q ``[batch, n_h, T, hd]``,
@@ -31,6 +33,14 @@ def _bind(path):
     lib.oracle_attention_rows.argtypes = [vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, i32, i32,
                                           f64, i32, i32, i32, i32, vp, vp]
     lib.oracle_attention_rows.restype = i32
+    lib.oracle_attention_rows_sink.argtypes = [vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, i32, i32,
+                                               f64, i32, i32, i32, i32, vp, vp, vp]
+    lib.oracle_attention_rows_sink.restype = i32
+    lib.oracle_attention_sink.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                          f64, i32, i32, i32, i32, vp, vp, vp]
+    lib.oracle_attention_sink.restype = i32
+    lib.oracle_merge_sink.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
+    lib.oracle_merge_sink.restype = None
     lib.oracle_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                      f64, i32, i32, i32, i32, vp, vp]
     lib.oracle_attention.restype = i32
@@ -80,26 +90,37 @@ def _check(q, k, v):
     return q, k, v, tq, (b, n_h, n_kv_h, T, s_k, hd)
 
 
-def attention(q, k, v, scale, window=0, causal=False, key_begin=0, key_end=None):
+def _sink_arg(sink, n_h):
+    if sink is None:
+        return None, None
+    sink = np.ascontiguousarray(np.asarray(sink, dtype=np.float64).reshape(-1))
+    if sink.size != n_h:
+        raise ValueError("sink must hold one logit per query head (%d), got %d" % (n_h, sink.size))
+    return sink, sink.ctypes.data
+
+
+def attention(q, k, v, scale, window=0, causal=False, key_begin=0, key_end=None, sink=None):
     """Return (O [b,n_h,T,hd] float64, lse [b,n_h,T] float64).
 
     ``key_begin``/``key_end`` restrict the attended keys to that half-open
-    range (one split-KV chunk); the default is every key."""
+    range (one split-KV chunk); the default is every key.  ``sink``: optional
+    [n_h] sink logits."""
     q, k, v, dt, (b, n_h, n_kv_h, T, s_k, hd) = _check(q, k, v)
     if key_end is None:
         key_end = s_k
+    sink, sink_p = _sink_arg(sink, n_h)
     o = np.empty((b, n_h, T, hd), np.float64)
     lse = np.empty((b, n_h, T), np.float64)
-    rc = _load().oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt,
-                                  b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
-                                  int(bool(causal)), int(key_begin), int(key_end),
-                                  o.ctypes.data, lse.ctypes.data)
+    rc = _load().oracle_attention_sink(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt,
+                                       b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
+                                       int(bool(causal)), int(key_begin), int(key_end), sink_p,
+                                       o.ctypes.data, lse.ctypes.data)
     if rc != 0:
         raise ValueError("oracle rejected the shape")
     return o, lse
 
 
-def attention_rows(q, k, v, rows, scale, window=0, causal=False, key_begin=0, key_end=None):
+def attention_rows(q, k, v, rows, scale, window=0, causal=False, key_begin=0, key_end=None, sink=None):
     """Attention for selected flattened rows ``((b*n_h)+h)*T+t``.
 
     Returns (O [len(rows), hd], lse [len(rows)]), float64."""
@@ -107,12 +128,14 @@ def attention_rows(q, k, v, rows, scale, window=0, causal=False, key_begin=0, ke
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     if key_end is None:
         key_end = s_k
+    sink, sink_p = _sink_arg(sink, n_h)
     o = np.empty((rows.size, hd), np.float64)
     lse = np.empty((rows.size,), np.float64)
-    rc = _load().oracle_attention_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt,
-                                       rows.ctypes.data, rows.size, b, n_h, n_kv_h, T, s_k, hd,
-                                       float(scale), int(window), int(bool(causal)),
-                                       int(key_begin), int(key_end), o.ctypes.data, lse.ctypes.data)
+    rc = _load().oracle_attention_rows_sink(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt,
+                                            rows.ctypes.data, rows.size, b, n_h, n_kv_h, T, s_k, hd,
+                                            float(scale), int(window), int(bool(causal)),
+                                            int(key_begin), int(key_end), sink_p, o.ctypes.data,
+                                            lse.ctypes.data)
     if rc != 0:
         raise ValueError("oracle rejected the rows or the shape")
     return o, lse
@@ -141,8 +164,10 @@ def partials(q, k, v, scale, kv_chunk, window=0, causal=False):
     return np.stack(os_), np.stack(ls_)
 
 
-def merge(o_parts, lse_parts):
-    """Merge split-KV partials: O [..., hd] float64 and lse [...] float64."""
+def merge(o_parts, lse_parts, sink=None):
+    """Merge split-KV partials: O [..., hd] float64 and lse [...] float64.
+
+    ``sink``: optional sink logit per output row (shape ``lse_parts.shape[1:]``)."""
     o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
     lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
     n = o_parts.shape[0]
@@ -152,8 +177,12 @@ def merge(o_parts, lse_parts):
         raise ValueError("o_parts [n,...,hd] and lse_parts [n,...] disagree")
     o = np.empty(o_parts.shape[1:], np.float64)
     lse = np.empty(lse_parts.shape[1:], np.float64)
-    _load().oracle_merge(o_parts.ctypes.data, lse_parts.ctypes.data, n, rows, hd,
-                         o.ctypes.data, lse.ctypes.data)
+    sink_p = None
+    if sink is not None:
+        sink = np.ascontiguousarray(np.broadcast_to(np.asarray(sink, dtype=np.float64), lse_parts.shape[1:]))
+        sink_p = sink.ctypes.data
+    _load().oracle_merge_sink(o_parts.ctypes.data, lse_parts.ctypes.data, n, rows, hd, sink_p,
+                              o.ctypes.data, lse.ctypes.data)
     return o, lse
 
 

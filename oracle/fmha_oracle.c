@@ -42,6 +42,15 @@
  *  - split-KV: chunk i covers keys [b0 + i*c, b0 + (i+1)*c) where
  *    b0 = first attended key of row t = 0 and c the chunk length; partial i
  *    is the same definition with J restricted to that chunk.
+ *  - attention sink: [C] lists "D5c sink" as a TODO and defines nothing.
+ *    Reading taken: a per-query-head logit sigma_h (natural-log units, the
+ *    same units as the scaled scores s_j) that enters the softmax
+ *    denominator only, as one more "key" whose value row is zero:
+ *        l   = sum_j exp(s_j - m) + exp(sigma_h - m),  m = max(max_j s_j, sigma_h)
+ *        O   = sum_j exp(s_j - m) v_j / l,   lse = m + ln(l)
+ *    so a row with no attended key has O = 0 and lse = sigma_h, and
+ *    sigma_h = -inf is no sink at all.  For split-KV the partials carry no
+ *    sink and the merge adds it once to its denominator.
  */
 #include <math.h>
 #include <stdint.h>
@@ -95,16 +104,17 @@ int oracle_split_layout(int T, int s_k, int window, int kv_chunk, int* begin)
     return (span + kv_chunk - 1) / kv_chunk;
 }
 
-/* One query row: the plain definition above over keys [j0, j1] (inclusive).
+/* One query row: the plain definition above over keys [j0, j1] (inclusive),
+ * with the sink logit `sink` (-INFINITY: none) in the denominator.
  * q_row/k_slab/v_slab are element offsets into the typed buffers. */
 static void attend_one_row(const void* q, size_t q_off, const void* k, const void* v,
                            size_t kv_off, int hd, double scale, int j0, int j1,
-                           int dtype, double* o_row, double* lse_out)
+                           int dtype, double sink, double* o_row, double* lse_out)
 {
     int d, j;
     if (j0 > j1) {
         for (d = 0; d < hd; ++d) o_row[d] = 0.0;
-        *lse_out = -INFINITY;
+        *lse_out = sink;  /* -inf without a sink */
         return;
     }
     int n = j1 - j0 + 1;
@@ -121,9 +131,11 @@ static void attend_one_row(const void* q, size_t q_off, const void* k, const voi
         s[j] = scale * dot;
         if (s[j] > m) m = s[j];
     }
-    /* softmax denominator l = sum_j exp(s_j - m) */
+    if (sink > m) m = sink;
+    /* softmax denominator l = sum_j exp(s_j - m) (+ exp(sink - m)) */
     double l = 0.0;
     for (j = 0; j < n; ++j) l += exp(s[j] - m);
+    if (sink != -INFINITY) l += exp(sink - m);
     /* O = sum_j softmax_j * v_j */
     for (d = 0; d < hd; ++d) o_row[d] = 0.0;
     for (j = 0; j < n; ++j) {
@@ -138,13 +150,13 @@ static void attend_one_row(const void* q, size_t q_off, const void* k, const voi
 
 /* Attention for an explicit list of flattened query rows
  * row = ((b * n_h) + h) * T + t.  o: [n_rows, hd], lse: [n_rows].
- * Keys are further restricted to [key_begin, key_end).  Returns 0, or -1 on
- * an invalid shape. */
-int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype,
-                          const int64_t* rows, int64_t n_rows,
-                          int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
-                          double scale, int window, int causal,
-                          int key_begin, int key_end, double* o, double* lse)
+ * Keys are further restricted to [key_begin, key_end).  sink: [n_h] sink
+ * logits, or NULL for none.  Returns 0, or -1 on an invalid shape. */
+int oracle_attention_rows_sink(const void* q, const void* k, const void* v, int dtype,
+                               const int64_t* rows, int64_t n_rows,
+                               int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                               double scale, int window, int causal,
+                               int key_begin, int key_end, const double* sink, double* o, double* lse)
 {
     if (batch < 0 || n_h <= 0 || n_kv_h <= 0 || n_h % n_kv_h != 0 || T < 0 || s_k < 0 || hd <= 0)
         return -1;
@@ -167,25 +179,45 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype
         size_t q_off = (size_t)r * (size_t)hd;
         size_t kv_off = ((size_t)b * n_kv_h + kvh) * (size_t)s_k * (size_t)hd;
         attend_one_row(q, q_off, k, v, kv_off, hd, scale, lo, hi, dtype,
-                       o + (size_t)i * hd, lse + i);
+                       sink ? sink[h] : -INFINITY, o + (size_t)i * hd, lse + i);
     }
     return bad ? -1 : 0;
 }
 
+/* oracle_attention_rows_sink without a sink. */
+int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype,
+                          const int64_t* rows, int64_t n_rows,
+                          int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                          double scale, int window, int causal,
+                          int key_begin, int key_end, double* o, double* lse)
+{
+    return oracle_attention_rows_sink(q, k, v, dtype, rows, n_rows, batch, n_h, n_kv_h, T, s_k, hd, scale,
+                                      window, causal, key_begin, key_end, NULL, o, lse);
+}
+
 /* Every row, keys restricted to [key_begin, key_end).  o: [batch, n_h, T, hd],
- * lse: [batch, n_h, T]. */
+ * lse: [batch, n_h, T].  sink: [n_h] or NULL. */
+int oracle_attention_sink(const void* q, const void* k, const void* v, int dtype,
+                          int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                          double scale, int window, int causal, int key_begin, int key_end,
+                          const double* sink, double* o, double* lse)
+{
+    int64_t n = (int64_t)batch * n_h * T, i;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    for (i = 0; i < n; ++i) rows[i] = i;
+    int rc = oracle_attention_rows_sink(q, k, v, dtype, rows, n, batch, n_h, n_kv_h, T, s_k, hd,
+                                        scale, window, causal, key_begin, key_end, sink, o, lse);
+    free(rows);
+    return rc;
+}
+
 int oracle_attention(const void* q, const void* k, const void* v, int dtype,
                      int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
                      double scale, int window, int causal, int key_begin, int key_end,
                      double* o, double* lse)
 {
-    int64_t n = (int64_t)batch * n_h * T, i;
-    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
-    for (i = 0; i < n; ++i) rows[i] = i;
-    int rc = oracle_attention_rows(q, k, v, dtype, rows, n, batch, n_h, n_kv_h, T, s_k, hd,
-                                   scale, window, causal, key_begin, key_end, o, lse);
-    free(rows);
-    return rc;
+    return oracle_attention_sink(q, k, v, dtype, batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal,
+                                 key_begin, key_end, NULL, o, lse);
 }
 
 /* Split-KV merge [B] "Next steps" item 4:
@@ -193,15 +225,19 @@ int oracle_attention(const void* q, const void* k, const void* v, int dtype,
  * evaluated with every exponent shifted by max_i lse_i (the same quotient,
  * kept in range).  A partial with lse_i = -inf has weight 0; if every partial
  * is empty the row is O = 0, lse = -inf.
+ * With a sink logit sigma (sink_rows[r], per output row; NULL: none) the
+ * denominator also holds exp(sigma) once: O = sum_i exp(lse_i) O_i /
+ * (sum_i exp(lse_i) + exp(sigma)), lse = ln(sum_i exp(lse_i) + exp(sigma)).
  * o_parts: [n_splits, rows, hd], lse_parts: [n_splits, rows]. */
-void oracle_merge(const double* o_parts, const double* lse_parts, int n_splits,
-                  int64_t rows, int hd, double* o, double* lse)
+void oracle_merge_sink(const double* o_parts, const double* lse_parts, int n_splits,
+                       int64_t rows, int hd, const double* sink_rows, double* o, double* lse)
 {
     int64_t r;
 #pragma omp parallel for schedule(static)
     for (r = 0; r < rows; ++r) {
         int i, d;
-        double mx = -INFINITY;
+        const double sg = sink_rows ? sink_rows[r] : -INFINITY;
+        double mx = sg;
         for (i = 0; i < n_splits; ++i)
             if (lse_parts[(size_t)i * rows + r] > mx) mx = lse_parts[(size_t)i * rows + r];
         double* orow = o + (size_t)r * hd;
@@ -209,6 +245,7 @@ void oracle_merge(const double* o_parts, const double* lse_parts, int n_splits,
         if (mx == -INFINITY) { lse[r] = -INFINITY; continue; }
         double den = 0.0;
         for (i = 0; i < n_splits; ++i) den += exp(lse_parts[(size_t)i * rows + r] - mx);
+        if (sg != -INFINITY) den += exp(sg - mx);
         for (i = 0; i < n_splits; ++i) {
             double w = exp(lse_parts[(size_t)i * rows + r] - mx) / den;
             const double* op = o_parts + ((size_t)i * rows + r) * hd;
@@ -216,6 +253,12 @@ void oracle_merge(const double* o_parts, const double* lse_parts, int n_splits,
         }
         lse[r] = mx + log(den);
     }
+}
+
+void oracle_merge(const double* o_parts, const double* lse_parts, int n_splits,
+                  int64_t rows, int hd, double* o, double* lse)
+{
+    oracle_merge_sink(o_parts, lse_parts, n_splits, rows, hd, NULL, o, lse);
 }
 
 void oracle_set_threads(int n)

@@ -6,7 +6,11 @@ brute-force evaluation on tiny shapes, invariants (softmax rows sum to one,
 uniform V returns V, key permutation invariance), closed forms (Q = 0 gives
 lse = ln|J| and the mean of the attended V rows; one dominant key returns its V
 row), split-KV merge equal to the single pass, and the unmasked case equal to
-``torch.softmax`` in float64.  ``test_pins_catch_planted_mistakes`` plants
+``torch.softmax`` in float64; with an attention sink (the reading the oracle
+states: one more logit in the denominator only) the same brute force with the
+sink's column, Q = 0 giving lse = ln(n + e^sigma), sigma = -inf equal to no
+sink, an empty key range giving lse = sigma, and the split merge adding the
+sink once.  ``test_pins_catch_planted_mistakes`` plants
 plausible mistakes in a copy of the oracle's C source and checks that the pins
 reject every one.
 """
@@ -40,7 +44,9 @@ def _arr(spec, n):
 # ----------------------------------------------------------------------------
 # independent brute force: materialise the score matrix and the mask matrix
 # ----------------------------------------------------------------------------
-def brute_force(q, k, v, scale, window, causal):
+def brute_force(q, k, v, scale, window, causal, sink=None):
+    """sink: optional [n_h] logits, one more column of the score matrix whose
+    value row is zero."""
     b, n_h, T, hd = q.shape
     _, n_kv_h, s_k, _ = k.shape
     G = n_h // n_kv_h
@@ -61,14 +67,15 @@ def brute_force(q, k, v, scale, window, causal):
                     if window > 0 and j <= pos - window:
                         ok = False
                     allowed[t, j] = ok
+            sg = -math.inf if sink is None else float(sink[h])
             for t in range(T):
                 idx = [j for j in range(s_k) if allowed[t, j]]
                 if not idx:
-                    lse[bi, h, t] = -math.inf
+                    lse[bi, h, t] = sg
                     continue
-                mx = max(S[t, j] for j in idx)
+                mx = max([S[t, j] for j in idx] + [sg])
                 e = {j: math.exp(S[t, j] - mx) for j in idx}
-                tot = sum(e.values())
+                tot = sum(e.values()) + (0.0 if sg == -math.inf else math.exp(sg - mx))
                 for d in range(hd):
                     o[bi, h, t, d] = sum(e[j] / tot * float(v[bi, kh, j, d]) for j in idx)
                 lse[bi, h, t] = mx + math.log(tot)
@@ -277,11 +284,93 @@ def pin_rows_api_matches_full():
     np.testing.assert_array_equal(lrow, lse.reshape(-1)[rows])
 
 
+SINKS = [None, "zero", "neg_inf", "big", "mixed"]
+
+
+def _sinks(kind, n_h, rng):
+    if kind is None:
+        return None
+    if kind == "zero":
+        return np.zeros(n_h)
+    if kind == "neg_inf":
+        return np.full(n_h, -np.inf)
+    if kind == "big":
+        return np.full(n_h, 30.0)  # dominates every score
+    return rng.standard_normal(n_h) * 2.0 + np.arange(n_h)  # a different logit per head
+
+
+def pin_sink_brute_force_tiny():
+    rng = np.random.default_rng(11)
+    for (b, n_h, n_kv_h, T, s_k, hd, window, causal) in TINY:
+        for kind in SINKS[1:]:
+            q = rng.standard_normal((b, n_h, T, hd))
+            k = rng.standard_normal((b, n_kv_h, s_k, hd)) * 2.0
+            v = rng.standard_normal((b, n_kv_h, s_k, hd))
+            sink = _sinks(kind, n_h, rng)
+            o, lse = oracle.attention(q, k, v, 0.7, window, causal, sink=sink)
+            ob, lb = brute_force(q, k, v, 0.7, window, causal, sink=sink)
+            np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12, err_msg=kind)
+            np.testing.assert_array_equal(np.isinf(lse), np.isinf(lb))
+            fin = np.isfinite(lb)
+            np.testing.assert_allclose(lse[fin], lb[fin], rtol=0, atol=1e-12, err_msg=kind)
+
+
+def pin_sink_q_zero_closed_form():
+    # all n scores 0: l = n + e^sigma, O = sum_j v_j / (n + e^sigma)
+    rng = np.random.default_rng(12)
+    n, hd = 9, 5
+    v = rng.standard_normal((1, 1, n, hd))
+    for sg in (-3.0, 0.0, 1.5, 20.0):
+        o, lse = oracle.attention(np.zeros((1, 1, 1, hd)), rng.standard_normal((1, 1, n, hd)), v, 0.3,
+                                  sink=[sg])
+        np.testing.assert_allclose(lse.ravel(), [math.log(n + math.exp(sg))], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o.ravel(), v.sum(axis=2).ravel() / (n + math.exp(sg)), rtol=0, atol=1e-12)
+
+
+def pin_sink_neg_inf_is_no_sink():
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((2, 4, 3, 8))
+    k = rng.standard_normal((2, 2, 11, 8))
+    v = rng.standard_normal((2, 2, 11, 8))
+    o0, l0 = oracle.attention(q, k, v, 0.4, 5, True)
+    o1, l1 = oracle.attention(q, k, v, 0.4, 5, True, sink=np.full(4, -np.inf))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+def pin_sink_empty_key_range():
+    # no attended key: O = 0 and lse = sigma (the sink alone is the denominator)
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((1, 3, 2, 4))
+    k = rng.standard_normal((1, 1, 6, 4))
+    sink = np.array([-1.0, 0.5, 7.0])
+    o, lse = oracle.attention(q, k, k, 1.0, key_begin=3, key_end=3, sink=sink)
+    np.testing.assert_array_equal(o, np.zeros_like(o))
+    np.testing.assert_array_equal(lse, np.repeat(sink[None, :, None], 2, axis=2))
+
+
+def pin_sink_split_merge_equals_single_pass():
+    # partials carry no sink; the merge adds it once
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((2, 4, 3, 6))
+    k = rng.standard_normal((2, 2, 40, 6)) * 1.5
+    v = rng.standard_normal((2, 2, 40, 6))
+    sink = rng.standard_normal(4) * 3.0
+    o1, l1 = oracle.attention(q, k, v, 0.5, 25, True, sink=sink)
+    rows_sink = np.broadcast_to(sink[None, :, None], l1.shape)
+    for chunk in (1, 7, 16, 40):
+        op, lp = oracle.partials(q, k, v, 0.5, chunk, 25, True)
+        om, lm = oracle.merge(op, lp, sink=rows_sink)
+        np.testing.assert_allclose(om, o1, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lm, l1, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_golden_cases, pin_brute_force_tiny, pin_softmax_rows_sum_to_one,
             pin_uniform_v_returns_v, pin_key_permutation_invariance, pin_q_zero_closed_form,
             pin_dominant_key, pin_single_attended_key, pin_split_merge_equals_single_pass,
             pin_split_layout, pin_torch_softmax_unmasked, pin_bf16_widening_is_exact,
-            pin_rows_api_matches_full]
+            pin_rows_api_matches_full, pin_sink_brute_force_tiny, pin_sink_q_zero_closed_form,
+            pin_sink_neg_inf_is_no_sink, pin_sink_empty_key_range, pin_sink_split_merge_equals_single_pass]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
@@ -304,6 +393,12 @@ MUTANTS = {
     "merge_plain_mean": ("double w = exp(lse_parts[(size_t)i * rows + r] - mx) / den;",
                          "double w = 1.0 / n_splits;"),
     "merge_lse_log2": ("lse[r] = mx + log(den);", "lse[r] = mx + log2(den);"),
+    "sink_unshifted": ("if (sink != -INFINITY) l += exp(sink - m);", "if (sink != -INFINITY) l += exp(sink);"),
+    "sink_per_kv_head": ("sink ? sink[h] : -INFINITY", "sink ? sink[kvh] : -INFINITY"),
+    "sink_empty_row_lse": ("*lse_out = sink;  /* -inf without a sink */", "*lse_out = -INFINITY;"),
+    "merge_sink_dropped": ("if (sg != -INFINITY) den += exp(sg - mx);", ";"),
+    "merge_sink_in_numerator": ("        if (sg != -INFINITY) den += exp(sg - mx);",
+                                "        if (sg != -INFINITY) { den += exp(sg - mx); orow[0] += exp(sg - mx); }"),
 }
 
 
