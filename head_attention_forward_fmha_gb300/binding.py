@@ -36,7 +36,8 @@ SIGNATURES = {
     "fmha_merge": ([_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "fmha_fwd_splitkv_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
                              _i32, _vp], _i32),
-    "fmha_merge_ex": ([_vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "fmha_merge_ex": ([_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "fmha_fwd_sink": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "fmha_splitkv_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32], _sz),
     "fmha_check_device_status": ([_vp], _i32),
     "fmha_get_last_error": ([], ctypes.c_char_p),
@@ -112,8 +113,17 @@ def _shapes(q, k, v):
     return b, n_h, n_kv_h, T, s_k, hd
 
 
-def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stream=None):
-    """O (bf16 [b,n_h,T,hd]) and LSE (fp32 [b,n_h,T]); allocates them if not given."""
+def _sink_ptr(sink, n_h):
+    if sink is None:
+        return None
+    if sink.numel() != n_h:
+        raise ValueError("sink must hold one logit per query head (%d), got %d" % (n_h, sink.numel()))
+    return _f32(sink, "sink")
+
+
+def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stream=None, sink=None):
+    """O (bf16 [b,n_h,T,hd]) and LSE (fp32 [b,n_h,T]); allocates them if not given.
+    sink: optional fp32 CUDA tensor of n_h attention-sink logits (fmha_fwd_sink)."""
     b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
     if o is None:
         o = torch.empty_like(q)
@@ -121,9 +131,16 @@ def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stre
         lse = torch.empty((b, n_h, T), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = hd ** -0.5
-    rc = load().fmha_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
-                         b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)), _stream(stream))
-    _check(rc, "fmha_fwd")
+    if sink is None:
+        rc = load().fmha_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                             b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)),
+                             _stream(stream))
+        _check(rc, "fmha_fwd")
+    else:
+        rc = load().fmha_fwd_sink(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                                  _sink_ptr(sink, n_h), b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
+                                  int(bool(causal)), _stream(stream))
+        _check(rc, "fmha_fwd_sink")
     return o, lse
 
 
@@ -170,8 +187,9 @@ def fmha_fwd_splitkv(q, k, v, kv_chunk, o_parts=None, lse_parts=None, scale=None
     return o_parts, lse_parts
 
 
-def fmha_merge(o_parts, lse_parts, o=None, lse=None, stream=None):
-    """Merge partials [n,b,n_h,T,hd] / [n,b,n_h,T] into bf16 O and fp32 LSE."""
+def fmha_merge(o_parts, lse_parts, o=None, lse=None, stream=None, sink=None):
+    """Merge partials [n,b,n_h,T,hd] / [n,b,n_h,T] into bf16 O and fp32 LSE
+    (with an optional [n_h] attention-sink tensor)."""
     if o_parts.dim() != 5 or lse_parts.dim() != 4 or tuple(o_parts.shape[:4]) != tuple(lse_parts.shape):
         raise ValueError("o_parts [n,b,n_h,T,hd] and lse_parts [n,b,n_h,T] expected")
     n, b, n_h, T, hd = o_parts.shape
@@ -179,9 +197,15 @@ def fmha_merge(o_parts, lse_parts, o=None, lse=None, stream=None):
         o = torch.empty((b, n_h, T, hd), dtype=torch.bfloat16, device=o_parts.device)
     if lse is None:
         lse = torch.empty((b, n_h, T), dtype=torch.float32, device=o_parts.device)
-    rc = load().fmha_merge(_f32(o_parts, "o_parts"), _f32(lse_parts, "lse_parts"), n, _bf16(o, "o"),
-                           _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
-    _check(rc, "fmha_merge")
+    if sink is None:
+        rc = load().fmha_merge(_f32(o_parts, "o_parts"), _f32(lse_parts, "lse_parts"), n, _bf16(o, "o"),
+                               _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
+        _check(rc, "fmha_merge")
+    else:
+        rc = load().fmha_merge_ex(_f32(o_parts, "o_parts"), _f32(lse_parts, "lse_parts"), None, PARTS_F32, n,
+                                  _sink_ptr(sink, n_h), _bf16(o, "o"), _f32(lse, "lse"), b, n_h, T, hd,
+                                  _stream(stream))
+        _check(rc, "fmha_merge_ex")
     return o, lse
 
 
@@ -211,7 +235,7 @@ def fmha_fwd_splitkv_f16(q, k, v, kv_chunk, o_parts=None, lse_parts=None, range_
     return o_parts, lse_parts, range_parts
 
 
-def fmha_merge_f16(o_parts, lse_parts, range_parts, o=None, lse=None, stream=None):
+def fmha_merge_f16(o_parts, lse_parts, range_parts, o=None, lse=None, stream=None, sink=None):
     """Merge FMHA_PARTS_F16 partials into bf16 O and fp32 LSE."""
     if o_parts.dim() != 5 or o_parts.dtype != torch.float16 or not o_parts.is_contiguous():
         raise ValueError("o_parts: contiguous fp16 [n,b,n_h,T,hd] expected")
@@ -223,7 +247,8 @@ def fmha_merge_f16(o_parts, lse_parts, range_parts, o=None, lse=None, stream=Non
     if lse is None:
         lse = torch.empty((b, n_h, T), dtype=torch.float32, device=o_parts.device)
     rc = load().fmha_merge_ex(o_parts.data_ptr(), _f32(lse_parts, "lse_parts"), _f32(range_parts, "range_parts"),
-                              PARTS_F16, n, _bf16(o, "o"), _f32(lse, "lse"), b, n_h, T, hd, _stream(stream))
+                              PARTS_F16, n, _sink_ptr(sink, n_h), _bf16(o, "o"), _f32(lse, "lse"), b, n_h, T, hd,
+                              _stream(stream))
     _check(rc, "fmha_merge_ex")
     return o, lse
 

@@ -283,9 +283,12 @@ int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long sla
 // Launch the kernel family the plan picks: O/LSE directly, or partials.
 // o_part is fp32, or fp16 with range_part when f16_parts (hd-512 tensor-core
 // kernel only).
+// sink: [n_h] attention-sink logits for the final output (NULL: none; never
+// applied to partials, whose merge adds it).
 int run_kernel(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
                float* lse, void* o_part, float* lse_part, bool to_partials, cudaStream_t stream,
-               bool f16_parts = false, float* range_part = nullptr) {
+               bool f16_parts = false, float* range_part = nullptr, const float* sink = nullptr) {
+    if (to_partials) sink = nullptr;
     unsigned* status = device_status_word();
     if (!status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
     const Path path = choose_path(p);
@@ -299,6 +302,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.lse_part = lse_part;
         L.range_part = range_part;
         L.to_partials = to_partials;
+        L.sink = sink;
         L.f16_partials = f16_parts;
         if (f16_parts && (path != Path::TensorCoreWide || !range_part || !to_partials))
             return fail(FMHA_ERR_LAUNCH, "fp16 partials need the hd-512 kernel and a range array");
@@ -327,6 +331,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
     L.o_part = static_cast<float*>(o_part);
     L.lse_part = lse_part;
     L.to_partials = to_partials;
+    L.sink = sink;
     L.p = p;
     L.sp = sp;
     L.status = status;
@@ -343,8 +348,9 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
 
 extern "C" {
 
-int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int n_h, int n_kv_h,
-             int T, int s_k, int hd, float scale, int window, int causal, fmha_stream_t stream) {
+int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* lse, const float* sink, int batch,
+                  int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                  fmha_stream_t stream) {
     try {
         Problem p;
         int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
@@ -353,12 +359,13 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         if (rc) return rc;
         if (!o || !lse) return fail(FMHA_ERR_NULL, "o and lse must be non-NULL");
         if (!aligned(o, 16) || !aligned(lse, 4)) return fail(FMHA_ERR_ALIGN, "o must be 16-byte, lse 4-byte aligned");
+        if (sink && !aligned(sink, 4)) return fail(FMHA_ERR_ALIGN, "sink must be 4-byte aligned");
         const long long rows = (long long)batch * n_h * T;
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = choose_split(p);
         if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
         if (sp.n_splits == 1)
-            return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
+            return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream, false, nullptr, sink);
         void* ws = nullptr;
         const bool f16 = use_f16_partials(p);
         rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits, f16), &ws);
@@ -366,13 +373,18 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         const PartialViews pv = partial_views(ws, rows, hd, sp.n_splits, f16);
         rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, pv.o_part, pv.lse_part, true, stream, f16, pv.range_part);
         if (rc) return rc;
-        cudaError_t e =
-            launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream);
+        cudaError_t e = launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream,
+                                     sink, T, n_h);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {
         return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd");
     }
+}
+
+int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int n_h, int n_kv_h,
+             int T, int s_k, int hd, float scale, int window, int causal, fmha_stream_t stream) {
+    return fmha_fwd_sink(q, k, v, o, lse, nullptr, batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, stream);
 }
 
 int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int window, int causal, int* kv_chunk,
@@ -436,7 +448,8 @@ int fmha_fwd_splitkv(const void* q, const void* k, const void* v, float* o_parts
 }
 
 int fmha_merge_ex(const void* o_parts, const float* lse_parts, const float* range_parts, int parts_format,
-                  int n_splits, void* o, float* lse, int batch, int n_h, int T, int hd, fmha_stream_t stream) {
+                  int n_splits, const float* sink, void* o, float* lse, int batch, int n_h, int T, int hd,
+                  fmha_stream_t stream) {
     if (hd != 64 && hd != 128 && hd != 256 && hd != 512)
         return fail(FMHA_ERR_HEADDIM, "hd=%d: supported head dims are 64, 128, 256, 512", hd);
     if (batch < 0 || n_h < 0 || T < 0 || n_splits < 1)
@@ -450,18 +463,19 @@ int fmha_merge_ex(const void* o_parts, const float* lse_parts, const float* rang
     if (!o_parts || !lse_parts || !o || !lse || (f16 && !range_parts))
         return fail(FMHA_ERR_NULL, "fmha_merge: NULL buffer");
     if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4) ||
-        (f16 && !aligned(range_parts, 4)))
-        return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse and range buffers 4-byte aligned");
+        (f16 && !aligned(range_parts, 4)) || (sink && !aligned(sink, 4)))
+        return fail(FMHA_ERR_ALIGN, "fmha_merge: o_parts and o 16-byte, lse, range and sink buffers 4-byte aligned");
     if (rows > (1LL << 32)) return fail(FMHA_ERR_SHAPE, "fmha_merge: too many rows");
     cudaError_t e = launch_merge(o_parts, lse_parts, f16 ? range_parts : nullptr, n_splits, rows, hd, f16, o, lse,
-                                 stream);
+                                 stream, sink, T, n_h);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FMHA_OK;
 }
 
 int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits, void* o, float* lse, int batch, int n_h,
                int T, int hd, fmha_stream_t stream) {
-    return fmha_merge_ex(o_parts, lse_parts, nullptr, FMHA_PARTS_F32, n_splits, o, lse, batch, n_h, T, hd, stream);
+    return fmha_merge_ex(o_parts, lse_parts, nullptr, FMHA_PARTS_F32, n_splits, nullptr, o, lse, batch, n_h, T, hd,
+                         stream);
 }
 
 size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits) {

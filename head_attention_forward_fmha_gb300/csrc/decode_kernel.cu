@@ -60,6 +60,7 @@ struct DecodeArgs {
     int kv_begin, kv_chunk;
     long long rows_total;  // batch * n_h * T
     unsigned* status;
+    const float* sink;     // [n_h] sink logits (final output only) or NULL
 };
 
 __device__ __forceinline__ void attended(int t, const DecodeArgs& a, int& lo, int& hi) {
@@ -316,8 +317,7 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         }
     named_barrier_sync(1, C::NCW * 32);
 
-    // Sum the key groups, divide once by the running sum, write out.
-    constexpr float kLn2 = 0.693147180559945309f;
+    // Sum the key groups, divide once by the running sum (plus the sink), write out.
     for (int item = threadIdx.x; item < C::RT * (HD / 8); item += C::NCW * 32) {
         const int r = item / (HD / 8), d8 = item - r * (HD / 8);
         if (r_begin + r >= r_end) continue;
@@ -328,7 +328,9 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         float L = 0.f;
 #pragma unroll
         for (int w = 0; w < C::KW; ++w) L += ml[w * C::RT + r].y * exp2f(ml[w * C::RT + r].x - Mu);
-        const float inv = (L > 0.f) ? 1.f / L : 0.f;
+        const long long grow = row0 + r_begin + r;
+        float inv, lse;
+        finish_row(M, L, a.to_partials ? -INFINITY : sink_log2(a.sink, grow, a.T, a.n_h), inv, lse);
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -339,8 +341,6 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
             acc[0] += u0.x; acc[1] += u0.y; acc[2] += u0.z; acc[3] += u0.w;
             acc[4] += u1.x; acc[5] += u1.y; acc[6] += u1.z; acc[7] += u1.w;
         }
-        const long long grow = row0 + r_begin + r;
-        const float lse = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
         if (!a.to_partials) {
             uint4 pk;
             pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -392,6 +392,7 @@ cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     a.kv_chunk = L.sp.kv_chunk;
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
+    a.sink = L.sink;
     const int row_tiles = (L.p.R + C::RT - 1) / C::RT;
     dim3 grid(row_tiles, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cudaLaunchConfig_t cfg = {};

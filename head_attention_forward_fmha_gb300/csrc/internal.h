@@ -29,6 +29,7 @@ struct DecodeLaunch {
     float* o_part;     // fp32 partial outputs (to_partials)
     float* lse_part;
     bool to_partials;
+    const float* sink;  // [n_h] attention-sink logits or NULL; applied when !to_partials
     CUtensorMap tmap_k, tmap_v;
     Problem p;
     SplitPlan sp;
@@ -46,6 +47,7 @@ struct TcLaunch {
     float* lse_part;
     float* range_part;  // fp16 partials only: [n_splits, rows, 2] power-of-two factor per row half
     bool to_partials;
+    const float* sink;  // [n_h] attention-sink logits or NULL; applied when !to_partials
     bool f16_partials;  // hd-512 kernel only
     CUtensorMap tmap_q, tmap_k, tmap_v;
     // bf16 O [slabs, R, hd] (box 64 x 128), fp32 partials [n_splits*slabs, R, hd]
@@ -77,8 +79,11 @@ inline cudaLaunchAttribute programmatic_launch_attr() {
 }
 
 // ---- split-KV merge (merge_kernel.cu) -------------------------------------
+// sink: [n_h] attention-sink logits added once to the merged denominator
+// (NULL: none); row r belongs to head (r / T) % n_h.
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                         long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream);
+                         long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream,
+                         const float* sink = nullptr, int T = 1, int n_h = 1);
 
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).

@@ -68,7 +68,8 @@ template <int HD, typename PT>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
                      const float* __restrict__ range_parts, int n_splits, long long rows,
-                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, const float* __restrict__ sink, int T,
+                     int n_h) {
     grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
     launch_dependents();     // the next kernel on the stream may start its set-up
     using C = MCfg<HD, PT>;
@@ -85,6 +86,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, __ldg(lse_parts + (long long)i * rows + row));
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    // attention sink: one more term exp(sigma) of the denominator (no value)
+    const float sg = sink ? __ldg(sink + (int)((row / T) % n_h)) : -INFINITY;
+    mx = fmaxf(mx, sg);
 
     float acc[V];
 #pragma unroll
@@ -128,6 +132,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
             }
         }
     }
+    if (sg != -INFINITY) den += exp2f((sg - mx) * kLog2e);
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
     __nv_bfloat16* dst = o + row * HD + col;
     if constexpr (V == 8) {
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 template <int HD, typename PT>
 cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                     long long rows, void* o, float* lse, cudaStream_t stream) {
+                     long long rows, void* o, float* lse, cudaStream_t stream, const float* sink, int T, int n_h) {
     const long long tasks = rows * MCfg<HD, PT>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
@@ -162,31 +167,34 @@ cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* ran
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT>, o_parts, lse_parts, range_parts, n_splits, rows,
-                              static_cast<__nv_bfloat16*>(o), lse);
+                              static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h);
 }
 
 template <int HD>
 cudaError_t launch_hd(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                      long long rows, bool f16, void* o, float* lse, cudaStream_t stream) {
+                      long long rows, bool f16, void* o, float* lse, cudaStream_t stream, const float* sink, int T,
+                      int n_h) {
     if (f16) {
         if (HD != 512 || range_parts == nullptr) return cudaErrorInvalidValue;
         return launch_t<HD>(static_cast<const __half*>(o_parts), lse_parts, range_parts, n_splits, rows, o, lse,
-                            stream);
+                            stream, sink, T, n_h);
     }
-    return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse,
-                        stream);
+    return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse, stream,
+                        sink, T, n_h);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                         long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream) {
+                         long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream,
+                         const float* sink, int T, int n_h) {
     if (rows <= 0) return cudaSuccess;
+    if (sink && (T < 1 || n_h < 1)) return cudaErrorInvalidValue;
     switch (hd) {
-        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
-        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
-        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
-        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream);
+        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
+        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
+        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
+        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
         default: return cudaErrorInvalidValue;
     }
 }

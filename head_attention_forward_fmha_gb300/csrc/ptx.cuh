@@ -174,6 +174,39 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// End of a row's online softmax: O = acc * inv and its natural-log LSE, from
+// the running max m and the sum l relative to it (both log2 units; l = 0 for
+// a row with no attended key).  sink_l2: the row's attention-sink logit in
+// log2 units (-inf: none), one more term of the denominator only:
+//   M = max(m, sink), l' = l 2^(m - M) + 2^(sink - M), inv = 2^(m - M) / l',
+//   lse = (M + log2 l') ln 2.
+// No attended key gives O = 0 and lse = sink (-inf without one).
+__device__ __forceinline__ void finish_row(float m, float l, float sink_l2, float& inv, float& lse) {
+    constexpr float kLn2 = 0.693147180559945309f;
+    if (!(l > 0.f)) {
+        inv = 0.f;
+        lse = sink_l2 * kLn2;
+        return;
+    }
+    if (sink_l2 == -INFINITY) {
+        inv = 1.f / l;
+        lse = (m + log2f(l)) * kLn2;
+        return;
+    }
+    const float M = fmaxf(m, sink_l2);
+    const float c = exp2f(m - M);
+    const float lt = l * c + exp2f(sink_l2 - M);
+    inv = c / lt;
+    lse = (M + log2f(lt)) * kLn2;
+}
+
+// A row's sink logit in log2 units: sink[h] * log2(e) for query head
+// h = (row / T) % n_h of the flattened row index, -inf without a sink array.
+__device__ __forceinline__ float sink_log2(const float* sink, long long row, int T, int n_h) {
+    if (!sink) return -INFINITY;
+    return __ldg(sink + (int)((row / T) % n_h)) * 1.4426950408889634f;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -77,6 +77,7 @@ struct TcArgs {
     int kv_begin, kv_chunk;
     long long rows_total;
     unsigned* status;
+    const float* sink;  // [n_h] sink logits (final output only) or NULL
 };
 
 __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, int& hi) {
@@ -325,9 +326,8 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
-        constexpr float kLn2 = 0.693147180559945309f;
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        float inv, lse;
+        finish_row(m_ref, l, a.to_partials ? -INFINITY : sink_log2(a.sink, row0 + grow, a.T, a.n_h), inv, lse);
         // O -> shared memory (the drained K/V stages) -> TMA store; rows past
         // the slab's end fall outside the tensor map and are not written.
         uint8_t* stage = sk;
@@ -386,6 +386,7 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     a.kv_chunk = L.sp.kv_chunk;
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
+    a.sink = L.sink;
     dim3 grid((L.p.R + C::BM - 1) / C::BM, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

@@ -60,6 +60,7 @@ struct WideArgs {
     int kv_begin, kv_chunk;
     long long rows_total;
     unsigned* status;
+    const float* sink;  // [n_h] sink logits (final output only) or NULL
 };
 
 __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, int& hi) {
@@ -318,9 +319,8 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
-        constexpr float kLn2 = 0.693147180559945309f;
-        float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        float inv, lse;
+        finish_row(m_ref, l, a.to_partials ? -INFINITY : sink_log2(a.sink, row0 + grow, a.T, a.n_h), inv, lse);
         const bool have_o = ok && n_tiles > 0;
         float range = 1.f;
         if (a.to_partials && a.part_f16) {
@@ -416,6 +416,7 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
     a.kv_chunk = L.sp.kv_chunk;
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
+    a.sink = L.sink;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cfg.blockDim = dim3(C::THREADS);

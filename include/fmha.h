@@ -170,10 +170,27 @@ int fmha_fwd_splitkv_ex(const void* q, const void* k, const void* v,
                         float scale, int window, int causal, fmha_stream_t stream);
 
 /* fmha_merge of partials in `parts_format` (range_parts as written by
- * fmha_fwd_splitkv_ex; FMHA_PARTS_F16 needs hd = 512). */
+ * fmha_fwd_splitkv_ex; FMHA_PARTS_F16 needs hd = 512), with an optional
+ * attention sink (see fmha_fwd_sink): sink is NULL or a device array of n_h
+ * fp32 logits, added once to each row's denominator. */
 int fmha_merge_ex(const void* o_parts, const float* lse_parts, const float* range_parts, int parts_format,
-                  int n_splits, void* o, float* lse, int batch, int n_h, int T, int hd,
+                  int n_splits, const float* sink, void* o, float* lse, int batch, int n_h, int T, int hd,
                   fmha_stream_t stream);
+
+/*
+ * fmha_fwd with an attention sink.  The pages list "D5c sink" as a TODO and
+ * define nothing; the reading taken here: query head h has a logit sigma_h
+ * (natural-log units, the same units as scale * q.k) that joins the softmax
+ * denominator only, as one more key whose value row is zero:
+ *     O   = sum_j exp(s_j) v_j / (sum_j exp(s_j) + exp(sigma_h))
+ *     LSE = ln(sum_j exp(s_j) + exp(sigma_h))
+ * A row with no attended key gets O = 0, LSE = sigma_h; sigma_h = -inf is no
+ * sink.  sink: device array of n_h fp32 logits, 4-byte aligned, caller-owned;
+ * NULL makes this call fmha_fwd.  Everything else as fmha_fwd.
+ */
+int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* lse, const float* sink,
+                  int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                  float scale, int window, int causal, fmha_stream_t stream);
 
 /* Bytes of fp32 partial output (o_parts + lse_parts) that fmha_fwd_splitkv
  * writes for n_splits chunks. */

@@ -120,9 +120,18 @@ def test_f16_partials_only_on_the_hd512_tensor_core_kernel(lib):
     assert f(16, 16, 16, 16, 16, 18, 1, 128, 1, 128, 1, 1, 256, 512, 0.1, 0, 0, None) == -2  # range misaligned
     assert f(16, 16, 16, 16, 16, 16, 7, 128, 1, 128, 1, 1, 256, 512, 0.1, 0, 0, None) == -5  # no such format
     m = lib.fmha_merge_ex
-    assert m(16, 16, 16, 1, 2, 16, 16, 1, 1, 1, 128, None) == -9
-    assert m(16, 16, 0, 1, 2, 16, 16, 1, 1, 1, 512, None) == -1
-    assert m(16, 16, 16, 1, 2, 16, 16, 0, 1, 1, 512, None) == 0                      # empty
+    assert m(16, 16, 16, 1, 2, None, 16, 16, 1, 1, 1, 128, None) == -9
+    assert m(16, 16, 0, 1, 2, None, 16, 16, 1, 1, 1, 512, None) == -1
+    assert m(16, 16, 16, 1, 2, None, 16, 16, 0, 1, 1, 512, None) == 0                # empty
+    assert m(16, 16, None, 0, 2, 18, 16, 16, 1, 1, 1, 64, None) == -2                # sink misaligned
+
+
+def test_fwd_sink_argument_errors(lib):
+    f = lib.fmha_fwd_sink
+    assert f(16, 16, 16, 16, 16, 18, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -2     # sink misaligned
+    assert f(16, 16, 16, 16, 16, 16, 1, 2, 1, 1, 8, 80, 0.125, 0, 0, None) == -3
+    assert f(16, 16, 16, 16, 16, 16, 0, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == 0      # empty problem
+
 
 
 def test_binding_refuses_missing_library(tmp_path):
