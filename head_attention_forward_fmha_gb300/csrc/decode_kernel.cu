@@ -71,7 +71,7 @@ __device__ __forceinline__ void attended(int t, const DecodeArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <int HD, int NB>
+template <int HD, int NB, bool SINK>
 __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                           const DecodeArgs a) {
@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         for (int w = 0; w < C::KW; ++w) L += ml[w * C::RT + r].y * exp2f(ml[w * C::RT + r].x - Mu);
         const long long grow = row0 + r_begin + r;
         float inv, lse;
-        finish_row(M, L, a.to_partials ? -INFINITY : sink_log2(a.sink, grow, a.T, a.n_h), inv, lse);
+        // query head of this row: kvh * G + (row within the slab) / T
+        finish_row(M, L, SINK ? sink_log2_of(a.sink, kvh * a.group + (r_begin + r) / a.T) : -INFINITY, inv, lse);
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -359,10 +360,10 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     }
 }
 
-template <int HD, int NB>
+template <int HD, int NB, bool SINK>
 cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     using C = DCfg<HD, NB>;
-    auto kern = decode_splitkv_kernel<HD, NB>;
+    auto kern = decode_splitkv_kernel<HD, NB, SINK>;
     static bool attr_set[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -412,15 +413,20 @@ int decode_kv_tile(int hd) { return hd <= 128 ? 64 : 32; }
 
 int decode_rows_per_cta(int hd, int R) { return (R > 8 && hd <= 256) ? 16 : 8; }
 
-cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
+template <bool SINK>
+cudaError_t launch_hd(const DecodeLaunch& L, cudaStream_t stream) {
     const bool two = decode_rows_per_cta(L.p.hd, L.p.R) == 16;
     switch (L.p.hd) {
-        case 64: return two ? launch_t<64, 2>(L, stream) : launch_t<64, 1>(L, stream);
-        case 128: return two ? launch_t<128, 2>(L, stream) : launch_t<128, 1>(L, stream);
-        case 256: return two ? launch_t<256, 2>(L, stream) : launch_t<256, 1>(L, stream);
-        case 512: return launch_t<512, 1>(L, stream);
+        case 64: return two ? launch_t<64, 2, SINK>(L, stream) : launch_t<64, 1, SINK>(L, stream);
+        case 128: return two ? launch_t<128, 2, SINK>(L, stream) : launch_t<128, 1, SINK>(L, stream);
+        case 256: return two ? launch_t<256, 2, SINK>(L, stream) : launch_t<256, 1, SINK>(L, stream);
+        case 512: return launch_t<512, 1, SINK>(L, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
+    return (L.sink && !L.to_partials) ? launch_hd<true>(L, stream) : launch_hd<false>(L, stream);
 }
 
 }  // namespace fmha

@@ -64,7 +64,7 @@ __device__ __forceinline__ void load_vec(const __half* p, float (&v)[VEC]) {
     }
 }
 
-template <int HD, typename PT>
+template <int HD, typename PT, bool SINK>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
                      const float* __restrict__ range_parts, int n_splits, long long rows,
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
     // attention sink: one more term exp(sigma) of the denominator (no value)
-    const float sg = sink ? __ldg(sink + (int)((row / T) % n_h)) : -INFINITY;
+    const float sg = SINK ? __ldg(sink + (int)((row / T) % n_h)) : -INFINITY;
     mx = fmaxf(mx, sg);
 
     float acc[V];
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
             }
         }
     }
-    if (sg != -INFINITY) den += exp2f((sg - mx) * kLog2e);
+    if (SINK && sg != -INFINITY) den += exp2f((sg - mx) * kLog2e);
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
     __nv_bfloat16* dst = o + row * HD + col;
     if constexpr (V == 8) {
@@ -166,7 +166,10 @@ cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* ran
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT>, o_parts, lse_parts, range_parts, n_splits, rows,
+    if (sink)
+        return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT, true>, o_parts, lse_parts, range_parts, n_splits,
+                                  rows, static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h);
+    return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT, false>, o_parts, lse_parts, range_parts, n_splits, rows,
                               static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h);
 }
 

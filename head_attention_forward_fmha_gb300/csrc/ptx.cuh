@@ -200,11 +200,10 @@ __device__ __forceinline__ void finish_row(float m, float l, float sink_l2, floa
     lse = (M + log2f(lt)) * kLn2;
 }
 
-// A row's sink logit in log2 units: sink[h] * log2(e) for query head
-// h = (row / T) % n_h of the flattened row index, -inf without a sink array.
-__device__ __forceinline__ float sink_log2(const float* sink, long long row, int T, int n_h) {
-    if (!sink) return -INFINITY;
-    return __ldg(sink + (int)((row / T) % n_h)) * 1.4426950408889634f;
+// Query head h's sink logit in log2 units.  The kernels take the sink as a
+// compile-time option, so that without one none of this code exists.
+__device__ __forceinline__ float sink_log2_of(const float* sink, int h) {
+    return __ldg(sink + h) * 1.4426950408889634f;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

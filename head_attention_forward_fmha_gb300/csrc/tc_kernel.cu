@@ -88,7 +88,7 @@ __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, i
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <int HD>
+template <int HD, bool SINK>
 __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const TcArgs a) {
@@ -327,7 +327,9 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
         float inv, lse;
-        finish_row(m_ref, l, a.to_partials ? -INFINITY : sink_log2(a.sink, row0 + grow, a.T, a.n_h), inv, lse);
+        // query head of this row: kvh * G + (row within the slab) / T
+        finish_row(m_ref, l, (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T) : -INFINITY, inv,
+                   lse);
         // O -> shared memory (the drained K/V stages) -> TMA store; rows past
         // the slab's end fall outside the tensor map and are not written.
         uint8_t* stage = sk;
@@ -354,10 +356,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     }
 }
 
-template <int HD>
+template <int HD, bool SINK>
 cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     using C = TCfg<HD>;
-    auto kern = fwd_tc_kernel<HD>;
+    auto kern = fwd_tc_kernel<HD, SINK>;
     static bool attr_set[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -412,13 +414,18 @@ int tc_kv_tile(int hd) {
 
 bool tc_supports(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
-cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream) {
+template <bool SINK>
+cudaError_t launch_hd(const TcLaunch& L, cudaStream_t stream) {
     switch (L.p.hd) {
-        case 64: return launch_t<64>(L, stream);
-        case 128: return launch_t<128>(L, stream);
-        case 256: return launch_t<256>(L, stream);
+        case 64: return launch_t<64, SINK>(L, stream);
+        case 128: return launch_t<128, SINK>(L, stream);
+        case 256: return launch_t<256, SINK>(L, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream) {
+    return (L.sink && !L.to_partials) ? launch_hd<true>(L, stream) : launch_hd<false>(L, stream);
 }
 
 }  // namespace fmha

@@ -71,6 +71,7 @@ __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
+template <bool SINK>
 __global__ void __launch_bounds__(WCfg::THREADS, 1)
     fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -320,7 +321,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
         float inv, lse;
-        finish_row(m_ref, l, a.to_partials ? -INFINITY : sink_log2(a.sink, row0 + grow, a.T, a.n_h), inv, lse);
+        // query head of this row: kvh * G + (row within the slab) / T
+        finish_row(m_ref, l, (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T) : -INFINITY, inv,
+                   lse);
         const bool have_o = ok && n_tiles > 0;
         float range = 1.f;
         if (a.to_partials && a.part_f16) {
@@ -385,14 +388,15 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
 int tc_wide_kv_tile() { return WCfg::BN; }
 
-cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
+template <bool SINK>
+cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     using C = WCfg;
     static bool attr_set[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<SINK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 128) attr_set[dev] = true;
     }
@@ -425,7 +429,11 @@ cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<SINK>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+}
+
+cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
+    return (L.sink && !L.to_partials) ? launch_wide_t<true>(L, stream) : launch_wide_t<false>(L, stream);
 }
 
 }  // namespace fmha
