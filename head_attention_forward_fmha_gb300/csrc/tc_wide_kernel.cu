@@ -12,6 +12,7 @@
 // chunks of this half.  TMEM: two S buffers (2 x 128 columns) + O half (256).
 // Softmax, lazy rescale and the epilogue are those of tc_kernel.cu; both
 // halves compute identical (max, sum), and half 0 writes the LSE.
+#include <algorithm>
 #include <climits>
 #include "internal.h"
 #include "ptx.cuh"
@@ -20,14 +21,21 @@
 namespace fmha {
 namespace {
 
-struct WCfg {
+// QRES = false: Q and K chunks stream through one 8-slot ring (a block with
+// a single KV tile reads Q once either way).  QRES = true (blocks with two or
+// more KV tiles): the 128 KB Q tile is loaded once and stays resident, and
+// only K and V chunks stream through a 4-slot ring; the epilogue then stages
+// O in the Q region.
+template <bool QRES>
+struct WCfgT {
     static constexpr int HD = 512;
     static constexpr int HALF = 256;
     static constexpr int BM = 128;
     static constexpr int BN = 128;
     static constexpr int SLOT_BYTES = 128 * 128;       // 128 rows x 64 bf16 columns
-    static constexpr int NSLOT = 8;
-    static constexpr int QK_ITEMS = 2 * (HD / 64);     // Q chunk + K chunk per column block
+    static constexpr int Q_CHUNKS = HD / 64;
+    static constexpr int NSLOT = QRES ? 4 : 8;
+    static constexpr int QK_ITEMS = QRES ? Q_CHUNKS : 2 * Q_CHUNKS;  // (Q chunk +) K chunk per column block
     static constexpr int V_ITEMS = HALF / 64;
     static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
     // The V items of a tile start at a multiple of V_ITEMS and never wrap the
@@ -38,15 +46,18 @@ struct WCfg {
     static constexpr int THREADS = 192;
     static constexpr int O_COL = 2 * BN;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int OFF_RING = 0;
-    static constexpr int OFF_P = NSLOT * SLOT_BYTES;
+    static constexpr int OFF_Q = 0;                                   // QRES: resident Q (128 KB)
+    static constexpr int OFF_RING = QRES ? Q_CHUNKS * SLOT_BYTES : 0;
+    static constexpr int OFF_P = OFF_RING + NSLOT * SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int N_BARS = 2 * NSLOT + 2 + 2;
+    static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging (128 KB)
+    static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + (QRES ? 1 : 0);
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(NSLOT * SLOT_BYTES >= BM * HALF * 4, "the epilogue stages fp32 O in the ring");
+    static_assert((QRES ? Q_CHUNKS : NSLOT) * SLOT_BYTES >= BM * HALF * 4, "the epilogue stages fp32 O");
 };
+using WCfg = WCfgT<false>;
 
 struct WideArgs {
     __nv_bfloat16* o;
@@ -71,12 +82,12 @@ __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <bool SINK>
+template <bool SINK, bool QRES>
 __global__ void __launch_bounds__(WCfg::THREADS, 1)
     fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                        const WideArgs a) {
-    using C = WCfg;
+    using C = WCfgT<QRES>;
     constexpr int BM = C::BM, BN = C::BN;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
@@ -89,6 +100,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     uint64_t* s_full = slot_empty + C::NSLOT;  // [2]
     uint64_t* p_ready = s_full + 2;
     uint64_t* o_done = p_ready + 1;
+    uint64_t* q_full = o_done + 1;  // QRES only
+    uint8_t* qres = smem + C::OFF_Q;
+    uint8_t* stage = smem + C::OFF_STAGE;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -123,21 +137,22 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
     // Producer item sequence: QK(0), then for each tile j: QK(j+1) (if any)
     // and V(j) -- the order the MMA warp consumes them in.  Item i -> kind
-    // (0 Q chunk, 1 K chunk, 2 V chunk), tile and 64-column chunk.
+    // (0 Q chunk, 1 K chunk, 2 V chunk), tile and 64-column chunk.  With a
+    // resident Q the QK items are K chunks only.
     const int n_items = n_tiles * C::TILE_ITEMS;
     auto item_of = [&](int i, int& kind, int& tile, int& c) {
         if (i < C::QK_ITEMS) {
             tile = 0;
-            kind = i & 1;
-            c = i >> 1;
+            kind = QRES ? 1 : (i & 1);
+            c = QRES ? i : (i >> 1);
             return;
         }
         const int r = i - C::QK_ITEMS;
         const int j = r / C::TILE_ITEMS, o = r - j * C::TILE_ITEMS;
         if (j < n_tiles - 1 && o < C::QK_ITEMS) {
             tile = j + 1;
-            kind = o & 1;
-            c = o >> 1;
+            kind = QRES ? 1 : (o & 1);
+            c = QRES ? o : (o >> 1);
         } else {
             tile = j;
             kind = 2;
@@ -169,6 +184,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         mbar_init(&s_full[1], 1);
         mbar_init(p_ready, 128);
         mbar_init(o_done, 1);
+        if (QRES) mbar_init(q_full, 1);
         *abort_flag = 0;
         mbar_fence_init();
         // The first ring-full needs no free slot: start it before the block
@@ -180,6 +196,11 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             pol_kv = l2_policy_evict_first();
             pol_q = l2_policy_evict_last();
             grid_dependency_wait();  // the preceding kernel's writes (Q, K, V) are visible
+            if (QRES) {
+                mbar_arrive_expect_tx(q_full, C::Q_CHUNKS * C::SLOT_BYTES);
+                for (int c = 0; c < C::Q_CHUNKS; ++c)
+                    tma_load_3d_hint(qres + c * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, q_full, pol_q);
+            }
             for (int i = 0; i < min(C::NSLOT, n_items); ++i) issue_item(i);
         }
     }
@@ -208,9 +229,10 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, C::HALF, 1);
-            const uint32_t ring_addr = smem_u32(ring), p_addr = smem_u32(sp);
+            const uint32_t ring_addr = smem_u32(ring), p_addr = smem_u32(sp), q_addr = smem_u32(qres);
             int item = 0;
             bool ok = true;
+            if (QRES) ok = mbar_wait(q_full, 0, a.status);
             auto slot_take = [&](int& s) -> bool {
                 s = item % C::NSLOT;
                 if (!mbar_wait(&slot_full[s], (item / C::NSLOT) & 1, a.status)) return false;
@@ -219,17 +241,19 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             };
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t d = tmem + (j & 1) * BN;
-                for (int c = 0; c < C::HD / 64; ++c) {
-                    int sq, sk;
-                    if (!slot_take(sq) || !slot_take(sk)) return false;
+                for (int c = 0; c < C::Q_CHUNKS; ++c) {
+                    int sq = 0, sk;
+                    if (!QRES && !slot_take(sq)) return false;
+                    if (!slot_take(sk)) return false;
                     tc_fence_after();
+                    const uint32_t a_base = QRES ? q_addr + c * C::SLOT_BYTES : ring_addr + sq * C::SLOT_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(ring_addr + sq * C::SLOT_BYTES + kk * 32, 16, 1024);
+                        const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(ring_addr + sk * C::SLOT_BYTES + kk * 32, 16, 1024);
                         tc_mma_f16(d, ad, bd, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(&slot_empty[sq]);
+                    if (!QRES) tc_commit(&slot_empty[sq]);
                     tc_commit(&slot_empty[sk]);
                 }
                 tc_commit(&s_full[j & 1]);
@@ -358,13 +382,13 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         // This half of O -> shared memory (the drained ring) -> TMA store.
         const int pslab = split * (int)(a.rows_total / a.R) + slab;
         if (!a.to_partials)
-            epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+            epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
                                                   slab, have_o, threadIdx.x == 64, abort_flag);
         else if (a.part_f16)
-            epilogue_tma_store<C::HALF, kOutF16>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+            epilogue_tma_store<C::HALF, kOutF16>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
                                                  pslab, have_o, threadIdx.x == 64, abort_flag);
         else
-            epilogue_tma_store<C::HALF, kOutF32>(t_lane + C::O_COL, inv, row, ring, &tmo, half * C::HALF, r_begin,
+            epilogue_tma_store<C::HALF, kOutF32>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
                                                  pslab, have_o, threadIdx.x == 64, abort_flag);
         if (valid && ok && half == 0) {
             const long long gr = row0 + grow;
@@ -388,15 +412,16 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
 int tc_wide_kv_tile() { return WCfg::BN; }
 
-template <bool SINK>
+template <bool SINK, bool QRES>
 cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
-    using C = WCfg;
+    using C = WCfgT<QRES>;
     static bool attr_set[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<SINK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<SINK, QRES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 128) attr_set[dev] = true;
     }
@@ -429,11 +454,18 @@ cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<SINK>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<SINK, QRES>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+}
+
+template <bool SINK>
+cudaError_t launch_wide_q(const TcLaunch& L, cudaStream_t stream) {
+    // Q stays resident when a block may see two or more 128-key tiles.
+    const int span = std::min(L.sp.kv_chunk, L.p.s_k);
+    return span > WCfg::BN ? launch_wide_t<SINK, true>(L, stream) : launch_wide_t<SINK, false>(L, stream);
 }
 
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
-    return (L.sink && !L.to_partials) ? launch_wide_t<true>(L, stream) : launch_wide_t<false>(L, stream);
+    return (L.sink && !L.to_partials) ? launch_wide_q<true>(L, stream) : launch_wide_q<false>(L, stream);
 }
 
 }  // namespace fmha
