@@ -169,11 +169,36 @@ KernelShape kernel_shape(const Problem& p, Path path) {
     return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2, 1, 256};
 }
 
+// Estimated time (us) of a tensor-core split into n chunks: waves of blocks
+// (one block per SM), each moving its K/V chunk, its Q tile and its output at
+// about 60 GB/s after ~1.5 us of fixed latency, never faster than all bytes at
+// the copy bandwidth, plus for n > 1 the merge (~2.5 us and its partials).
+// The constants are this GPU's measured per-block rates (GB300: a 128-row
+// block streams ~60-75 GB/s; block set-up, softmax tail and epilogue ~1.5 us).
+double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long long units, long long sms,
+                     long long span, long long n) {
+    const long long ctas = units * n;
+    const long long waves = (ctas + sms - 1) / sms;
+    long long keys = (span + n - 1) / n;
+    keys = (keys + ks.kv_tile - 1) / ks.kv_tile * ks.kv_tile;
+    // bytes per key: K and V rows (the hd-512 blocks read all of K, half of V)
+    const double kv = (double)keys * (wide ? 3.0 * p.hd : 4.0 * p.hd);
+    const double q = (double)ks.rows_per_cta * p.hd * 2.0;
+    const double part_b = n > 1 ? (wide ? 2.0 : 4.0) : 2.0;
+    const double out = (double)ks.rows_per_cta * (p.hd / ks.blocks_per_row_tile) * part_b;
+    const double block_us = 1.5 + (kv + q + out) / 60e3;
+    double t = (double)waves * block_us;
+    const double floor_us = (double)ctas * (kv + q + out) / 6.7e6;
+    if (t < floor_us) t = floor_us;
+    if (n > 1) t += 2.5 + (double)p.batch * p.n_h * p.T * p.hd * part_b * (double)n / 10e6;
+    return t;
+}
+
 // Split heuristic.  Decode kernel: enough thread blocks to fill every SM a few
 // times over (its partials are small next to the K/V it streams).  Tensor-core
-// kernels: split only when the row tiles cannot fill half the GPU, and then
-// only up to one wave, since their fp32 partials (128 rows x hd per chunk)
-// cost about as much traffic as the K/V chunk itself.
+// kernels (one block per SM): the chunk count with the least estimated time
+// (tc_split_cost), which weighs wave quantisation against the Q tile each
+// extra block reloads and the partials it writes.
 SplitPlan choose_split(const Problem& p) {
     const Path path = choose_path(p);
     const KernelShape ks = kernel_shape(p, path);
@@ -182,17 +207,27 @@ SplitPlan choose_split(const Problem& p) {
     SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
     const long long span = (long long)p.s_k - whole.kv_begin;
     const long long sms = sm_count();
-    long long target;
+    if (units <= 0 || span <= ks.min_chunk) return whole;
+    long long n = 1;
     if (path != Path::Decode) {
-        if (units * 2 >= sms) return whole;
-        target = sms;
+        const bool wide = path == Path::TensorCoreWide;
+        long long max_n = span / ks.min_chunk;
+        if (max_n > 64) max_n = 64;
+        double best = tc_split_cost(p, ks, wide, units, sms, span, 1);
+        for (long long c = 2; c <= max_n; ++c) {
+            const double t = tc_split_cost(p, ks, wide, units, sms, span, c);
+            if (t < best * 0.97) {  // a clear gain only: fewer chunks on near-ties
+                best = t;
+                n = c;
+            }
+        }
     } else {
-        target = 4LL * sms * ks.ctas_per_sm;
+        const long long target = 4LL * sms * ks.ctas_per_sm;
+        if (units >= target) return whole;
+        n = (target + units - 1) / units;
+        const long long max_n = span / ks.min_chunk;
+        if (n > max_n) n = max_n;
     }
-    if (units <= 0 || span <= ks.min_chunk || units >= target) return whole;
-    long long n = (target + units - 1) / units;
-    const long long max_n = span / ks.min_chunk;
-    if (n > max_n) n = max_n;
     if (n <= 1) return whole;
     long long chunk = (span + n - 1) / n;
     chunk = (chunk + ks.kv_tile - 1) / ks.kv_tile * ks.kv_tile;
