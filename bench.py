@@ -17,8 +17,10 @@ timed alone, against the measured HBM copy bandwidth), ``cpu_baseline`` (the
 fp64 oracle on the host cores, a bounded sample), ``e2e`` (host buffers:
 pinned H2D copies + fmha_fwd + D2H of O and LSE per step), ``clocks``
 (nvidia-smi sampled during the timed region), ``gpu_launches`` and
-``secondary`` (the GQA sliding-window decode with 512-key split + merge, and
-the causal prefill, each with its own roofline figures).
+``secondary`` (the GQA sliding-window decode, and the causal prefill, each with
+its own roofline figures, as ``fmha_fwd`` plans them; for the GQA decode also
+``split_512``: the same workload split literally into 512-key chunks with
+``fmha_fwd_splitkv`` + ``fmha_merge``).
 
 ``--impl reference`` times the fp64 oracle on the host cores instead (the only
 reference implementation this project has), on the same workload and metric.
@@ -336,6 +338,31 @@ def measure_kernel_only(binding, w, sets, stream, steps):
     return out
 
 
+def run_explicit_split(binding, w, chunk, steps, stream):
+    """ms per step of fmha_fwd_splitkv (chunks of `chunk` keys) + fmha_merge,
+    graph-replayed over rotating inputs (> 2x L2)."""
+    sets, _ = rotating_sets(w, 2)
+    _, n = binding.fmha_split_layout(w.T, w.s_k, w.window, chunk)
+    parts = []
+    for _s in sets:
+        op = torch.empty((n, w.batch, w.n_h, w.T, w.hd), dtype=torch.float32, device="cuda")
+        lp = torch.empty((n, w.batch, w.n_h, w.T), dtype=torch.float32, device="cuda")
+        parts.append((op, lp))
+
+    def step(i):
+        q, k, v, o, lse = sets[i]
+        binding.fmha_fwd_splitkv(q, k, v, chunk, parts[i][0], parts[i][1], scale=w.scale, window=w.window,
+                                 causal=w.causal, stream=stream)
+        binding.fmha_merge(parts[i][0], parts[i][1], o, lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i % len(sets))
+    ms = graph_time(step, len(sets), steps, stream) / steps
+    binding.fmha_check_device_status(stream)
+    return ms, n
+
+
 def run_workload(binding, w, steps, warmup, stream, dist=None, sampler=None):
     sets, l2 = rotating_sets(w, 2)
 
@@ -401,7 +428,7 @@ def run_e2e(binding, w, steps, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline(w, budget_s=12.0):
+def cpu_baseline(w, budget_s=15.0):
     """The fp64 oracle on the host cores over a bounded sample of the workload."""
     import numpy as np
     import oracle
@@ -468,7 +495,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the MHA shape sweep, one JSON line per point (not the bench line)")
     args = ap.parse_args()
@@ -538,6 +565,12 @@ def main():
                 "traffic": recorded_traffic(r2["kernel"], name),
                 "steps": st,
             }
+            if chunk:
+                ms_c, n_c = run_explicit_split(binding, w2, chunk, st, stream)
+                secondary[name]["split_%d" % chunk] = {
+                    "ms_per_step": round(ms_c, 5), "n_splits": n_c,
+                    "GB/s": round(b2 / (ms_c * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(b2 / (ms_c * 1e-3) / 1e9 / hbm_peak, 4)}
     sampler.stop()
 
     n = world

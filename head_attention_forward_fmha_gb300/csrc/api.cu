@@ -194,8 +194,10 @@ double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long lo
     return t;
 }
 
-// Split heuristic.  Decode kernel: enough thread blocks to fill every SM a few
-// times over (its partials are small next to the K/V it streams).  Tensor-core
+// Split heuristic.  Decode kernel: as many chunks as keep every thread block
+// resident in one wave (SMs x blocks per SM); a chunk scan on GB300 (MHA b4
+// h16, hd 64-512, s_k 4096-32768, and the GQA window decode) found the step
+// fastest there, longer chunks amortising each block's fixed latency.  Tensor-core
 // kernels (one block per SM): the chunk count with the least estimated time
 // (tc_split_cost), which weighs wave quantisation against the Q tile each
 // extra block reloads and the partials it writes.
@@ -222,9 +224,9 @@ SplitPlan choose_split(const Problem& p) {
             }
         }
     } else {
-        const long long target = 4LL * sms * ks.ctas_per_sm;
+        const long long target = sms * ks.ctas_per_sm;
         if (units >= target) return whole;
-        n = (target + units - 1) / units;
+        n = target / units;
         const long long max_n = span / ks.min_chunk;
         if (n > max_n) n = max_n;
     }

@@ -18,11 +18,11 @@ pytestmark = pytest.mark.gpu
 
 W = inputs.Workload
 
-# Shapes that fmha_fwd splits, so the scratch array is really used: the GQA
-# sliding-window decode (decode kernel) and an MQA decode with many cached
-# keys (tensor-core kernel).
+# Shapes that fmha_fwd splits, so the scratch array is really used: a GQA
+# sliding-window decode with few KV heads (decode kernel) and an MQA decode
+# with many cached keys (tensor-core kernel).
 SPLIT_SHAPES = [
-    inputs.WORKLOADS["gqa_swa_decode"],
+    W("gqa_swa_decode_b4", 4, 64, 8, 1, 8192, 128, window=4096),
     W("mqa_G128_hd128_long", 2, 128, 1, 1, 4096, 128),
 ]
 
@@ -64,16 +64,18 @@ def test_noalloc_unsplit_shape_needs_no_scratch():
 
 
 def test_noalloc_rejects_partials_larger_than_the_scratch():
-    # Decode-kernel shape with just under four waves of 16-row thread blocks on
-    # this GPU: the plan splits 512 keys in two, and the fp32 partials of
-    # ~19k query rows at hd 256 need about 40 MB, more than the scratch.
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    w = W("oversize", 4 * sms * 2 - 1, 16, 1, 1, 512, 256)
+    # MHA prefill at hd 512, 100 heads, 4096 cached keys: the plan splits the
+    # keys in two, and the fp32 partials of 12,800 query rows need ~52 MB, more
+    # than the scratch.  The call is refused before anything runs, so the
+    # inputs need no values.
+    w = W("oversize", 1, 100, 100, 128, 4096, 512)
     n_splits, _ = _plan(w)
     need = binding.fmha_splitkv_workspace_bytes(w.batch, w.n_h, w.T, w.hd, n_splits)
     if need <= binding.NOALLOC_SCRATCH_BYTES:
         pytest.skip("this GPU's plan for the shape fits the scratch (%d bytes)" % need)
-    q, k, v = inputs.make_inputs(w, seed=24, device="cuda")
+    q = torch.empty((w.batch, w.n_h, w.T, w.hd), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((w.batch, w.n_kv_h, w.s_k, w.hd), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
     o = torch.zeros_like(q)
     lse = torch.zeros((w.batch, w.n_h, w.T), dtype=torch.float32, device="cuda")
     with pytest.raises(binding.FmhaError) as ei:
