@@ -199,3 +199,47 @@ def test_back_to_back_calls_see_previous_output(w):
         o_ref, lse_ref = oracle_full(w, src, k, v)
         compare(outs[i], lses[i], o_ref, lse_ref, "%s call %d" % (w.name, i))
         src = outs[i].cpu()
+
+
+def _random_shapes(n, seed):
+    """Seeded random small shapes over every knob: batch, heads and grouping,
+    T, s_k (ragged), hd, window and causal."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        hd = int(rng.choice([64, 128, 256, 512]))
+        n_kv_h = int(rng.choice([1, 2, 4]))
+        G = int(rng.choice([1, 2, 8, 16, 64]))
+        T = int(rng.choice([1, 2, 3, 8, 33, 128]))
+        causal = bool(rng.random() < 0.4)
+        s_k = int(rng.integers(max(T, 1) if causal else 1, 700))
+        window = int(rng.choice([0, 0, 1, 17, 256]))
+        b = int(rng.integers(1, 3))
+        out.append(W("rand%d_hd%d_G%d_T%d_sk%d_w%d_c%d" % (i, hd, G, T, s_k, window, causal), b, n_kv_h * G,
+                     n_kv_h, T, s_k, hd, window=window, causal=causal))
+    return out
+
+
+RANDOM = _random_shapes(24, 2024)
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM)), ids=[w.name for w in RANDOM])
+def test_random_shapes_match_oracle(i):
+    """fmha_fwd under the automatic plan and, rotating, each forced kernel
+    family; then an explicit split into seeded chunk lengths plus the merge."""
+    w = RANDOM[i]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=51)
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    try:
+        binding.fmha_set_kernel_path(i % 3)
+        o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+        chunk = int(np.random.default_rng(i).integers(16, 320))
+        op, lp = binding.fmha_fwd_splitkv(qd, kd, vd, chunk, scale=w.scale, window=w.window, causal=w.causal)
+        om, lm = binding.fmha_merge(op, lp)
+        torch.cuda.synchronize()
+    finally:
+        binding.fmha_set_kernel_path(0)
+    binding.fmha_check_device_status()
+    compare(o, lse, o_ref, lse_ref, "%s path %d" % (w.name, i % 3))
+    cosine_per_head(o, o_ref, w.name)
+    compare(om, lm, o_ref, lse_ref, "%s split %d" % (w.name, chunk))
