@@ -11,15 +11,17 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-# FMHA_GB300_LIB may name another build of the same library (for example one
-# compiled with different tile parameters) to load instead of the in-tree one.
+# FMHA_GB300_LIB may name another build of the same library (for example the
+# checked build, CHECKED_LIB_PATH) to load instead of the in-tree one.
 LIB_PATH = os.environ.get("FMHA_GB300_LIB") or os.path.join(_PKG, "libfmha_gb300.so")
+CHECKED_LIB_PATH = os.path.join(_PKG, "libfmha_gb300_checked.so")
+FMHA_BUILD_CHECKED = 1
 
 FMHA_OK = 0
 ERRORS = {
     -1: "FMHA_ERR_NULL", -2: "FMHA_ERR_ALIGN", -3: "FMHA_ERR_HEADDIM", -4: "FMHA_ERR_HEADS",
     -5: "FMHA_ERR_SHAPE", -6: "FMHA_ERR_WORKSPACE", -7: "FMHA_ERR_LAUNCH", -8: "FMHA_ERR_DEVICE_TIMEOUT",
-    -9: "FMHA_ERR_UNSUPPORTED",
+    -9: "FMHA_ERR_UNSUPPORTED", -10: "FMHA_ERR_DEVICE_BOUNDS",
 }
 # Partial formats (enum fmha_parts_format).
 PARTS_F32, PARTS_F16 = 0, 1
@@ -46,6 +48,8 @@ SIGNATURES = {
     "fmha_set_kernel_path": ([_i32], _i32),
     "fmha_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i32),
     "fmha_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
+    "fmha_build_flags": ([], _i32),
+    "fmha_selftest_bounds_check": ([_vp], _i32),
 }
 # Size of the fixed split-KV scratch fmha_fwd_noalloc uses (FMHA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -272,6 +276,16 @@ def fmha_release():
 
 def fmha_version():
     return int(load().fmha_version())
+
+
+def fmha_build_flags():
+    """FMHA_BUILD_CHECKED if the loaded library is the checked build, else 0."""
+    return int(load().fmha_build_flags())
+
+
+def fmha_selftest_bounds_check(stream=None):
+    """One failing index check on the device (recorded only by the checked build)."""
+    _check(load().fmha_selftest_bounds_check(_stream(stream)), "fmha_selftest_bounds_check")
 
 
 def fmha_selftest_wait_timeout(timeout_us, stream=None):

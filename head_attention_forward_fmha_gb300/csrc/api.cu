@@ -525,16 +525,21 @@ int fmha_check_device_status(fmha_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     unsigned* w = device_status_word();
     if (!w) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
-    unsigned h = 0;
-    e = cudaMemcpy(&h, w, sizeof h, cudaMemcpyDeviceToHost);
+    unsigned h[2] = {0u, 0u};
+    e = cudaMemcpy(h, w, sizeof h, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-    if (h) {
+    if (h[0] || h[1]) {
         e = cudaMemset(w, 0, sizeof h);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
-        return fail(FMHA_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", h);
+        if (h[0] & fmha::kStatusBitBounds)
+            return fail(FMHA_ERR_DEVICE_BOUNDS, "an index check failed at site 0x%x (%s); status 0x%x", h[1],
+                        fmha::check_site_name(h[1]), h[0]);
+        return fail(FMHA_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", h[0]);
     }
     return FMHA_OK;
 }
+
+int fmha_build_flags(void) { return fmha::checked_build() ? FMHA_BUILD_CHECKED : 0; }
 
 const char* fmha_get_last_error(void) { return g_last_error.c_str(); }
 
@@ -559,6 +564,12 @@ int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream) {
         return fail(FMHA_ERR_SHAPE, "timeout_us must be in [1, 10^7] (got %u)", timeout_us);
     cudaError_t e = launch_wait_timeout_selftest((unsigned long long)timeout_us * 1000ull, stream);
     if (e != cudaSuccess) return cuda_fail(e, "wait-timeout self-test launch");
+    return FMHA_OK;
+}
+
+int fmha_selftest_bounds_check(fmha_stream_t stream) {
+    cudaError_t e = launch_bounds_check_selftest(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "index-check self-test launch");
     return FMHA_OK;
 }
 

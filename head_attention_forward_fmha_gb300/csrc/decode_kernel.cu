@@ -126,8 +126,12 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
             for (int it = 0; it < n_tiles; ++it) {
                 const int s = it % C::STAGES;
                 if (it >= C::STAGES && !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, a.status)) break;
-                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
                 const int key = k_lo + it * C::KT;
+                if (!FMHA_IN_BOUNDS(key >= 0 && key < k_hi && k_hi <= a.s_k && s < C::STAGES &&
+                                        slab < (int)gridDim.z,
+                                    kSiteDecKVLoad, a.status))
+                    break;
+                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
                 uint8_t* kst = stages + s * C::STAGE_BYTES;
                 uint8_t* vst = kst + C::TILE_BYTES;
 #pragma unroll
@@ -147,9 +151,11 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     for (int i = threadIdx.x; i < C::RT * (HD / 8); i += C::NCW * 32) {
         const int r = i / (HD / 8), c8 = i - r * (HD / 8);
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (r_begin + r < r_end)
+        if (r_begin + r < r_end &&
+            FMHA_IN_BOUNDS(row0 + r_begin + r >= 0 && row0 + r_begin + r < a.rows_total, kSiteDecQRow, a.status))
             val = *reinterpret_cast<const uint4*>(a.q + (row0 + r_begin + r) * HD + c8 * 8);
-        *reinterpret_cast<uint4*>(qs + r * C::Q_STRIDE + c8 * 16) = val;
+        if (FMHA_IN_BOUNDS(r * C::Q_STRIDE + c8 * 16 + 16 <= C::Q_BYTES, kSiteDecQSmem, a.status))
+            *reinterpret_cast<uint4*>(qs + r * C::Q_STRIDE + c8 * 16) = val;
     }
 
     // Attended key interval of each accumulator row this thread holds
@@ -182,7 +188,8 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
 
     named_barrier_sync(1, C::NCW * 32);  // Q staged
 
-    const uint32_t q_addr = smem_u32(qs) + ((lane & 7) + (NB == 2 ? 8 * (lane >> 4) : 0)) * C::Q_STRIDE +
+    const uint32_t qs_addr = smem_u32(qs);
+    const uint32_t q_addr = qs_addr + ((lane & 7) + (NB == 2 ? 8 * (lane >> 4) : 0)) * C::Q_STRIDE +
                             ((lane >> 3) & 1) * 16;
     const int k_row = 16 * kw + (lane & 15);
     const int k_c8 = lane >> 4;
@@ -206,14 +213,18 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
             const int d = 16 * kk + 8 * k_c8;
-            const uint32_t ka = kst + (d >> 6) * C::BOX_BYTES + k_row * 128 + ((((d & 63) >> 3) ^ (k_row & 7)) << 4);
+            uint32_t ka = kst + (d >> 6) * C::BOX_BYTES + k_row * 128 + ((((d & 63) >> 3) ^ (k_row & 7)) << 4);
+            if (!FMHA_IN_BOUNDS(ka >= kst && ka + 16 <= kst + C::TILE_BYTES, kSiteDecLdsmK, a.status)) ka = kst;
             uint32_t a0, a1, a2, a3;
             ldsm_x4(ka, a0, a1, a2, a3);
+            uint32_t qa = q_addr + kk * 32;
+            if (!FMHA_IN_BOUNDS(qa >= qs_addr && qa + 16 <= qs_addr + C::Q_BYTES, kSiteDecLdsmQ, a.status))
+                qa = qs_addr;
             uint32_t bq[NB][2];
             if constexpr (NB == 1) {
-                ldsm_x2(q_addr + kk * 32, bq[0][0], bq[0][1]);
+                ldsm_x2(qa, bq[0][0], bq[0][1]);
             } else {
-                ldsm_x4(q_addr + kk * 32, bq[0][0], bq[0][1], bq[1][0], bq[1][1]);
+                ldsm_x4(qa, bq[0][0], bq[0][1], bq[1][0], bq[1][1]);
             }
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sc[nb], a0, a1, a2, a3, bq[nb][0], bq[nb][1]);
@@ -265,7 +276,8 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
 #pragma unroll
         for (int db = 0; db < C::HDW / 16; ++db) {
             const int d = dw * C::HDW + 16 * db + 8 * v_c8;
-            const uint32_t va = vst + (d >> 6) * C::BOX_BYTES + v_row * 128 + ((((d & 63) >> 3) ^ (v_row & 7)) << 4);
+            uint32_t va = vst + (d >> 6) * C::BOX_BYTES + v_row * 128 + ((((d & 63) >> 3) ^ (v_row & 7)) << 4);
+            if (!FMHA_IN_BOUNDS(va >= vst && va + 16 <= vst + C::TILE_BYTES, kSiteDecLdsmV, a.status)) va = vst;
             uint32_t a0, a1, a2, a3;
             ldsm_x4_t(va, a0, a1, a2, a3);
 #pragma unroll
@@ -293,7 +305,11 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int i = 0; i < 2; ++i) ml[kw * C::RT + nb * 8 + 2 * lane + i] = make_float2(m[nb][i], l[nb][i]);
+            for (int i = 0; i < 2; ++i) {
+                const int mi = kw * C::RT + nb * 8 + 2 * lane + i;
+                if (FMHA_IN_BOUNDS(mi >= 0 && mi < C::KW * C::RT, kSiteDecMl, a.status))
+                    ml[mi] = make_float2(m[nb][i], l[nb][i]);
+            }
     }
     named_barrier_sync(1, C::NCW * 32);
 
@@ -311,8 +327,10 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
 #pragma unroll
             for (int db = 0; db < C::HDW / 16; ++db) {
                 const int d = dw * C::HDW + 16 * db + (lane >> 2);
-                comb[(kw * C::RT + r) * HD + d] = o[db][nb][i] * f;
-                comb[(kw * C::RT + r) * HD + d + 8] = o[db][nb][2 + i] * f;
+                const int ci = (kw * C::RT + r) * HD + d;
+                if (!FMHA_IN_BOUNDS(ci >= 0 && ci + 8 < C::KW * C::RT * HD, kSiteDecComb, a.status)) continue;
+                comb[ci] = o[db][nb][i] * f;
+                comb[ci + 8] = o[db][nb][2 + i] * f;
             }
         }
     named_barrier_sync(1, C::NCW * 32);
@@ -331,7 +349,8 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         const long long grow = row0 + r_begin + r;
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
-        finish_row(M, L, SINK ? sink_log2_of(a.sink, kvh * a.group + (r_begin + r) / a.T) : -INFINITY, inv, lse);
+        finish_row(M, L, SINK ? sink_log2_of(a.sink, kvh * a.group + (r_begin + r) / a.T, a.n_h, a.status) : -INFINITY,
+                   inv, lse);
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -342,6 +361,8 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
             acc[0] += u0.x; acc[1] += u0.y; acc[2] += u0.z; acc[3] += u0.w;
             acc[4] += u1.x; acc[5] += u1.y; acc[6] += u1.z; acc[7] += u1.w;
         }
+        if (!FMHA_IN_BOUNDS(grow >= 0 && grow < a.rows_total && split < (int)gridDim.y, kSiteDecOut, a.status))
+            continue;
         if (!a.to_partials) {
             uint4 pk;
             pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);

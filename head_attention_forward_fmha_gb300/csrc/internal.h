@@ -88,7 +88,14 @@ cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const floa
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).
 unsigned* device_status_word();
+// status[0] bits (kStatusBarrierTimeout = 1, kStatusBoundsViolation = 2) and
+// the description of a site code of a checked build's index check.
+constexpr unsigned kStatusBitTimeout = 1u, kStatusBitBounds = 2u;
+const char* check_site_name(unsigned site);
+bool checked_build();  // compiled with -DFMHA_CHECKED
 // Launch a kernel whose bounded wait must time out after limit_ns.
 cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);
+// Launch a kernel that runs one failing index check (a no-op unless checked).
+cudaError_t launch_bounds_check_selftest(cudaStream_t stream);
 
 }  // namespace fmha

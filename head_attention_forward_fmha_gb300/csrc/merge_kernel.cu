@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
                      const float* __restrict__ range_parts, int n_splits, long long rows,
                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse, const float* __restrict__ sink, int T,
-                     int n_h) {
+                     int n_h, unsigned* status) {
     grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
     launch_dependents();     // the next kernel on the stream may start its set-up
     using C = MCfg<HD, PT>;
@@ -79,6 +79,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     if (task >= rows * C::NSLICE) return;
     const long long row = task / C::NSLICE;
     const int col = (int)(task - row * C::NSLICE) * C::SLICE + lane * V;
+    if constexpr (kCheckedBuild) {  // the warp leaves together: shuffles follow
+        const bool in = FMHA_IN_BOUNDS(row >= 0 && row < rows && col >= 0 && col + V <= HD, kSiteMergeOut, status);
+        if (!__all_sync(0xffffffffu, in)) return;
+    }
     constexpr float kLog2e = 1.4426950408889634f;
     constexpr float kLn2 = 0.693147180559945309f;
 
@@ -87,7 +91,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
     // attention sink: one more term exp(sigma) of the denominator (no value)
-    const float sg = SINK ? __ldg(sink + (int)((row / T) % n_h)) : -INFINITY;
+    const int head = (int)((row / T) % n_h);
+    const float sg = (SINK && FMHA_IN_BOUNDS(head >= 0 && head < n_h, kSiteMergeSink, status)) ? __ldg(sink + head)
+                                                                                               : -INFINITY;
     mx = fmaxf(mx, sg);
 
     float acc[V];
@@ -102,13 +108,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                 (mine < n_splits) ? exp2f((__ldg(lse_parts + (long long)mine * rows + row) - mx) * kLog2e) : 0.f;
             float w_mine = w_den;  // weight of the stored values (times the range factor for fp16)
             if constexpr (sizeof(PT) == 2) {
-                if (mine < n_splits) w_mine *= __ldg(range_parts + ((long long)mine * rows + row) * 2 + col / 256);
+                if (mine < n_splits && FMHA_IN_BOUNDS(col / 256 < 2, kSiteMergeRange, status))
+                    w_mine *= __ldg(range_parts + ((long long)mine * rows + row) * 2 + col / 256);
             }
             float wsum = w_den;
 #pragma unroll
             for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
             den += wsum;
             const int cnt = min(32, n_splits - base);
+            if (!FMHA_IN_BOUNDS(cnt > 0 && base + cnt <= n_splits, kSiteMergePart, status)) break;
             int i = 0;
             for (; i + 4 <= cnt; i += 4) {
                 float v0[V], v1[V], v2[V], v3[V];
@@ -155,7 +163,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 template <int HD, typename PT>
 cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
-                     long long rows, void* o, float* lse, cudaStream_t stream, const float* sink, int T, int n_h) {
+                     long long rows, void* o, float* lse, cudaStream_t stream, const float* sink, int T, int n_h,
+                     unsigned* status) {
     const long long tasks = rows * MCfg<HD, PT>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
@@ -168,22 +177,22 @@ cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* ran
     cfg.numAttrs = 1;
     if (sink)
         return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT, true>, o_parts, lse_parts, range_parts, n_splits,
-                                  rows, static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h);
+                                  rows, static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h, status);
     return cudaLaunchKernelEx(&cfg, merge_lse_kernel<HD, PT, false>, o_parts, lse_parts, range_parts, n_splits, rows,
-                              static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h);
+                              static_cast<__nv_bfloat16*>(o), lse, sink, T, n_h, status);
 }
 
 template <int HD>
 cudaError_t launch_hd(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
                       long long rows, bool f16, void* o, float* lse, cudaStream_t stream, const float* sink, int T,
-                      int n_h) {
+                      int n_h, unsigned* status) {
     if (f16) {
         if (HD != 512 || range_parts == nullptr) return cudaErrorInvalidValue;
         return launch_t<HD>(static_cast<const __half*>(o_parts), lse_parts, range_parts, n_splits, rows, o, lse,
-                            stream, sink, T, n_h);
+                            stream, sink, T, n_h, status);
     }
     return launch_t<HD>(static_cast<const float*>(o_parts), lse_parts, nullptr, n_splits, rows, o, lse, stream,
-                        sink, T, n_h);
+                        sink, T, n_h, status);
 }
 
 }  // namespace
@@ -193,11 +202,13 @@ cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const floa
                          const float* sink, int T, int n_h) {
     if (rows <= 0) return cudaSuccess;
     if (sink && (T < 1 || n_h < 1)) return cudaErrorInvalidValue;
+    unsigned* status = device_status_word();
+    if (!status) return cudaErrorInvalidDevicePointer;
     switch (hd) {
-        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
-        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
-        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
-        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h);
+        case 64: return launch_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h, status);
+        case 128: return launch_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h, status);
+        case 256: return launch_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h, status);
+        case 512: return launch_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, o, lse, stream, sink, T, n_h, status);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -15,9 +15,79 @@ namespace fmha {
 // ---------------------------------------------------------------------------
 // device status word (see status.cu); bit values
 // ---------------------------------------------------------------------------
+// The word is status[0]; status[1] holds the site code of the first failed
+// index check of a checked build.
 enum : unsigned {
-    kStatusBarrierTimeout = 1u,  // a bounded mbarrier wait gave up
+    kStatusBarrierTimeout = 1u,   // a bounded mbarrier wait gave up
+    kStatusBoundsViolation = 2u,  // checked build: an index check failed and its access was skipped
 };
+
+// ---------------------------------------------------------------------------
+// checked builds
+// ---------------------------------------------------------------------------
+// A library compiled with -DFMHA_CHECKED tests, before the access, every
+// computed shared-memory offset, tensor-memory column, global-memory index
+// and TMA coordinate of the kernels against the extent of its buffer.  A
+// failed check sets kStatusBoundsViolation, records its site code in
+// status[1] (the first failure wins) and the access does not happen: a plain
+// load or store is skipped, a warp-collective instruction (ldmatrix,
+// tcgen05.ld/st) is pointed at offset 0 of its buffer instead.  A wrong index
+// therefore shows up in fmha_check_device_status() and never as a fault; a
+// skipped TMA load leaves its barrier short of bytes, so the consumer's
+// bounded wait gives up as well.  In normal builds FMHA_IN_BOUNDS() is the
+// constant true and its condition is not evaluated.
+#ifdef FMHA_CHECKED
+constexpr bool kCheckedBuild = true;
+#else
+constexpr bool kCheckedBuild = false;
+#endif
+
+// Site codes: 0x1nn row-tile kernel, 0x2nn hd-512 kernel, 0x3nn decode
+// kernel, 0x4nn merge, 0x5nn shared epilogue / softmax helpers.
+enum CheckSite : unsigned {
+    kSiteTcQLoad = 0x101,   // Q box coordinates
+    kSiteTcKLoad = 0x102,   // K tile: first key, stage offset
+    kSiteTcVLoad = 0x103,   // V tile: first key, stage offset
+    kSiteTcKDesc = 0x104,   // K stage the QK MMA reads
+    kSiteTcVDesc = 0x105,   // V stage and P buffer the PV MMA reads
+    kSiteTcSCol = 0x106,    // TMEM columns of the S buffer
+    kSiteTcPRow = 0x107,    // row of the P buffer
+    kSiteTcLse = 0x108,     // LSE / partial LSE index
+    kSiteWideItem = 0x201,  // ring slot and box coordinates of a producer item
+    kSiteWideQ = 0x202,     // resident-Q box coordinates
+    kSiteWideVSlots = 0x203,  // the V_ITEMS slots of a PV MMA are consecutive
+    kSiteWideQKDesc = 0x204,  // Q and K slots the QK MMA reads
+    kSiteWideSCol = 0x205,
+    kSiteWidePRow = 0x206,
+    kSiteWideLse = 0x207,
+    kSiteWideRange = 0x208,  // range factor index of an fp16 partial
+    kSiteDecQRow = 0x301,    // Q row loaded from global memory
+    kSiteDecQSmem = 0x302,   // Q staging offset
+    kSiteDecKVLoad = 0x303,  // K/V stage: first key, stage offset
+    kSiteDecLdsmK = 0x304,   // ldmatrix address inside the K tile
+    kSiteDecLdsmQ = 0x305,   // ldmatrix address inside the Q rows
+    kSiteDecLdsmV = 0x306,   // ldmatrix address inside the V tile
+    kSiteDecComb = 0x307,    // combine buffer index
+    kSiteDecMl = 0x308,      // per-key-group (max, sum) index
+    kSiteDecOut = 0x309,     // output / partial row
+    kSiteMergePart = 0x401,  // partial (split, row, column) index
+    kSiteMergeRange = 0x402,
+    kSiteMergeOut = 0x403,
+    kSiteMergeSink = 0x404,
+    kSiteEpiRow = 0x501,     // staging row of the TMA-store epilogue
+    kSiteEpiStore = 0x502,   // TMA store box coordinates
+    kSiteSink = 0x503,       // sink logit head index
+    kSiteSelfTest = 0x601,   // fmha_selftest_bounds_check (no access behind it)
+};
+
+static __device__ __noinline__ bool bounds_failed(unsigned site, unsigned* status) {
+    atomicOr(status, kStatusBoundsViolation);
+    atomicCAS(status + 1, 0u, site);
+    return false;
+}
+
+#define FMHA_IN_BOUNDS(cond, site, status) \
+    (!::fmha::kCheckedBuild || (cond) || ::fmha::bounds_failed((site), (status)))
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -202,7 +272,8 @@ __device__ __forceinline__ void finish_row(float m, float l, float sink_l2, floa
 
 // Query head h's sink logit in log2 units.  The kernels take the sink as a
 // compile-time option, so that without one none of this code exists.
-__device__ __forceinline__ float sink_log2_of(const float* sink, int h) {
+__device__ __forceinline__ float sink_log2_of(const float* sink, int h, int n_h, unsigned* status) {
+    if (!FMHA_IN_BOUNDS(h >= 0 && h < n_h, kSiteSink, status)) return -INFINITY;
     return __ldg(sink + h) * 1.4426950408889634f;
 }
 

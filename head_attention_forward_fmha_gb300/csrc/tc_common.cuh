@@ -103,14 +103,19 @@ enum OutMode : int {
 // Boxes are stored as soon as they are staged, so the TMA reads box b while
 // the threads stage box b + 1; only the last read is waited for.
 // have_o must be uniform within each warp (tcgen05.ld is warp-collective);
-// if any thread set *abort_flag, nothing is stored.
+// if any thread set *abort_flag, nothing is stored.  `ext` = the tensor map's
+// (columns, rows, slabs) extents and `stage_bytes` the staging space, both
+// only read by the index checks of a checked build.
 template <int NCOL, int MODE>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, int row, uint8_t* stage,
-                                                   const void* tmap, int col0, int row0_coord, int slab_coord,
-                                                   bool have_o, bool leader, const int* abort_flag) {
+                                                   int stage_bytes, const void* tmap, int col0, int row0_coord,
+                                                   int slab_coord, int3 ext, bool have_o, bool leader,
+                                                   const int* abort_flag, unsigned* status) {
     constexpr bool F32 = MODE == kOutF32;
     constexpr int BOX_COLS = F32 ? 32 : 64;
     constexpr int CHUNKS_PER_BOX = BOX_COLS / 32;
+    const bool row_ok = FMHA_IN_BOUNDS(row >= 0 && row < 128 && (NCOL / BOX_COLS) * 16384 <= stage_bytes,
+                                       kSiteEpiRow, status);
 #pragma unroll 1
     for (int bx = 0; bx < NCOL / BOX_COLS; ++bx) {
 #pragma unroll
@@ -125,6 +130,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, in
                 for (int i = 0; i < 32; ++i) ov[i] = 0.f;
             }
             uint8_t* rowp = stage + bx * 16384 + row * 128;
+            if (!row_ok) continue;
             if constexpr (F32) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -154,8 +160,12 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, in
         }
         fence_proxy_async_smem();
         named_barrier_sync(2, 128);
-        if (leader && *abort_flag == 0) {
-            tma_store_3d(tmap, col0 + bx * BOX_COLS, row0_coord, slab_coord, stage + bx * 16384);
+        const int c0 = col0 + bx * BOX_COLS;
+        if (leader && *abort_flag == 0 &&
+            FMHA_IN_BOUNDS(c0 >= 0 && c0 % BOX_COLS == 0 && c0 + BOX_COLS <= ext.x && row0_coord >= 0 &&
+                               row0_coord < ext.y && slab_coord >= 0 && slab_coord < ext.z,
+                           kSiteEpiStore, status)) {
+            tma_store_3d(tmap, c0, row0_coord, slab_coord, stage + bx * 16384);
             tma_store_commit();
         }
     }

@@ -182,18 +182,21 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         if (lane == 0 && n_tiles > 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+            if (FMHA_IN_BOUNDS(r_begin >= 0 && r_begin < a.R && slab < (int)gridDim.z, kSiteTcQLoad, a.status)) {
+                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
+                for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
+            }
             const uint64_t pol = l2_policy_evict_first();
             for (int j = 0; j < n_tiles; ++j) {
                 const int s = j % KST;
                 if (j >= KST && !mbar_wait(&k_empty[s], ((j / KST) - 1) & 1, a.status)) break;
+                const int key = k_lo + j * BN;
+                if (!FMHA_IN_BOUNDS(key >= 0 && key < k_hi && k_hi <= a.s_k && s < KST, kSiteTcKLoad, a.status)) break;
                 mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c)
-                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, k_lo + j * BN, slab,
-                                     &k_full[s], pol);
+                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, key, slab, &k_full[s], pol);
             }
         }
     } else if (warp == 6) {
@@ -204,11 +207,12 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             for (int j = 0; j < n_tiles; ++j) {
                 const int s = j % VST;
                 if (j >= VST && !mbar_wait(&v_empty[s], ((j / VST) - 1) & 1, a.status)) break;
+                const int key = k_lo + j * BN;
+                if (!FMHA_IN_BOUNDS(key >= 0 && key < k_hi && k_hi <= a.s_k && s < VST, kSiteTcVLoad, a.status)) break;
                 mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c)
-                    tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, k_lo + j * BN, slab,
-                                     &v_full[s], pol);
+                    tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, key, slab, &v_full[s], pol);
             }
         }
     } else if (warp == 1) {
@@ -222,6 +226,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             bool ok = mbar_wait(q_full, 0, a.status);
             auto issue_qk = [&](int j) -> bool {
                 const int s = j % KST;
+                if (!FMHA_IN_BOUNDS(s >= 0 && s < KST, kSiteTcKDesc, a.status)) return false;
                 if (!mbar_wait(&k_full[s], (j / KST) & 1, a.status)) return false;
                 tc_fence_after();
                 const uint32_t d = tmem + C::S_COL0 + (j & 1) * BN;
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % VST;
                 const int pb = j & 1;
+                if (!FMHA_IN_BOUNDS(s >= 0 && s < VST && pb < 2, kSiteTcVDesc, a.status)) break;
                 if (!mbar_wait(&p_ready[pb], (j >> 1) & 1, a.status)) break;
                 if (!mbar_wait(&v_full[s], (j / VST) & 1, a.status)) break;
                 tc_fence_after();
@@ -279,10 +285,13 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             }
             tc_fence_after();
             float x[BN];
+            const uint32_t s_col = FMHA_IN_BOUNDS(C::S_COL0 + (j & 1) * BN + BN <= C::O_COL, kSiteTcSCol, a.status)
+                                       ? C::S_COL0 + (j & 1) * BN
+                                       : 0u;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 float v32[32];
-                tmem_ld32(t_lane + C::S_COL0 + (j & 1) * BN + c * 32, v32);
+                tmem_ld32(t_lane + s_col + c * 32, v32);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
             }
@@ -303,7 +312,8 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                     break;
                 }
             }
-            write_p_row<BN>(sp + pb * C::P_BYTES, row, x);
+            if (FMHA_IN_BOUNDS(row >= 0 && row < BM && pb < 2, kSiteTcPRow, a.status))
+                write_p_row<BN>(sp + pb * C::P_BYTES, row, x);
             if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
@@ -328,24 +338,30 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         tc_fence_after();
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
-        finish_row(m_ref, l, (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T) : -INFINITY, inv,
-                   lse);
+        finish_row(m_ref, l,
+                   (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T, a.n_h, a.status) : -INFINITY,
+                   inv, lse);
         // O -> shared memory (the drained K/V stages) -> TMA store; rows past
         // the slab's end fall outside the tensor map and are not written.
         uint8_t* stage = sk;
+        constexpr int kStageBytes = (KST + VST) * C::KV_TILE;
         if (!a.to_partials)
-            epilogue_tma_store<HD, kOutBf16>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin, slab,
-                                          ok && n_tiles > 0, threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<HD, kOutBf16>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo, 0, r_begin,
+                                             slab, make_int3(HD, a.R, (int)gridDim.z), ok && n_tiles > 0,
+                                             threadIdx.x == 64, abort_flag, a.status);
         else
-            epilogue_tma_store<HD, kOutF32>(t_lane + C::O_COL, inv, row, stage, &tmo, 0, r_begin,
-                                         split * (int)(a.rows_total / a.R) + slab, ok && n_tiles > 0,
-                                         threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<HD, kOutF32>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo, 0, r_begin,
+                                            split * (int)(a.rows_total / a.R) + slab,
+                                            make_int3(HD, a.R, (int)(gridDim.y * gridDim.z)), ok && n_tiles > 0,
+                                            threadIdx.x == 64, abort_flag, a.status);
         if (valid && ok) {
             const long long gr = row0 + grow;
-            if (!a.to_partials)
-                a.lse[gr] = lse;
-            else
-                a.lse_part[(long long)split * a.rows_total + gr] = lse;
+            if (FMHA_IN_BOUNDS(gr >= 0 && gr < a.rows_total && split < (int)gridDim.y, kSiteTcLse, a.status)) {
+                if (!a.to_partials)
+                    a.lse[gr] = lse;
+                else
+                    a.lse_part[(long long)split * a.rows_total + gr] = lse;
+            }
         }
         tc_fence_before();
     }

@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         item_of(i, kind, tile, c);
         const int s = i % C::NSLOT;
         const int key = k_lo + tile * BN;
+        const bool in_range = kind == 0 ? (r_begin >= 0 && r_begin < a.R && c >= 0 && c < C::Q_CHUNKS)
+                            : kind == 1 ? (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::Q_CHUNKS)
+                                        : (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::V_ITEMS);
+        if (!FMHA_IN_BOUNDS(in_range && s >= 0 && s < C::NSLOT && slab < (int)gridDim.z, kSiteWideItem, a.status))
+            return;
         mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
         uint8_t* dst = ring + s * C::SLOT_BYTES;
         if (kind == 0)
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             pol_kv = l2_policy_evict_first();
             pol_q = l2_policy_evict_last();
             grid_dependency_wait();  // the preceding kernel's writes (Q, K, V) are visible
-            if (QRES) {
+            if (QRES && FMHA_IN_BOUNDS(r_begin >= 0 && r_begin < a.R && slab < (int)gridDim.z, kSiteWideQ, a.status)) {
                 mbar_arrive_expect_tx(q_full, C::Q_CHUNKS * C::SLOT_BYTES);
                 for (int c = 0; c < C::Q_CHUNKS; ++c)
                     tma_load_3d_hint(qres + c * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, q_full, pol_q);
@@ -245,6 +250,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                     int sq = 0, sk;
                     if (!QRES && !slot_take(sq)) return false;
                     if (!slot_take(sk)) return false;
+                    if (!FMHA_IN_BOUNDS(sq >= 0 && sq < C::NSLOT && sk >= 0 && sk < C::NSLOT, kSiteWideQKDesc,
+                                        a.status))
+                        return false;
                     tc_fence_after();
                     const uint32_t a_base = QRES ? q_addr + c * C::SLOT_BYTES : ring_addr + sq * C::SLOT_BYTES;
 #pragma unroll
@@ -269,6 +277,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                     int sv;
                     ok = slot_take(sv);
                     if (c == 0) sv0 = sv;
+                    if (ok) ok = FMHA_IN_BOUNDS(sv == sv0 + c && sv < C::NSLOT, kSiteWideVSlots, a.status);
                 }
                 if (!ok) break;
                 tc_fence_after();
@@ -307,10 +316,12 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             }
             tc_fence_after();
             float x[BN];
+            const uint32_t s_col =
+                FMHA_IN_BOUNDS((j & 1) * BN + BN <= C::O_COL, kSiteWideSCol, a.status) ? (j & 1) * BN : 0u;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 float v32[32];
-                tmem_ld32(t_lane + (j & 1) * BN + c * 32, v32);
+                tmem_ld32(t_lane + s_col + c * 32, v32);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
             }
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 ok = false;
                 break;
             }
-            write_p_row<BN>(sp, row, x);
+            if (FMHA_IN_BOUNDS(row >= 0 && row < BM, kSiteWidePRow, a.status)) write_p_row<BN>(sp, row, x);
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 tc_fence_after();
 #pragma unroll 1
@@ -346,8 +357,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         tc_fence_after();
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
-        finish_row(m_ref, l, (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T) : -INFINITY, inv,
-                   lse);
+        finish_row(m_ref, l,
+                   (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T, a.n_h, a.status) : -INFINITY,
+                   inv, lse);
         const bool have_o = ok && n_tiles > 0;
         float range = 1.f;
         if (a.to_partials && a.part_f16) {
@@ -381,24 +393,32 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         }
         // This half of O -> shared memory (the drained ring) -> TMA store.
         const int pslab = split * (int)(a.rows_total / a.R) + slab;
+        constexpr int kStageBytes = (QRES ? C::Q_CHUNKS : C::NSLOT) * C::SLOT_BYTES;
+        const int3 ext = make_int3(C::HD, a.R, (int)(a.to_partials ? gridDim.y * gridDim.z : gridDim.z));
         if (!a.to_partials)
-            epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
-                                                  slab, have_o, threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo,
+                                                  half * C::HALF, r_begin, slab, ext, have_o, threadIdx.x == 64,
+                                                  abort_flag, a.status);
         else if (a.part_f16)
-            epilogue_tma_store<C::HALF, kOutF16>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
-                                                 pslab, have_o, threadIdx.x == 64, abort_flag);
+            epilogue_tma_store<C::HALF, kOutF16>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo,
+                                                 half * C::HALF, r_begin, pslab, ext, have_o, threadIdx.x == 64,
+                                                 abort_flag, a.status);
         else
-            epilogue_tma_store<C::HALF, kOutF32>(t_lane + C::O_COL, inv, row, stage, &tmo, half * C::HALF, r_begin,
-                                                 pslab, have_o, threadIdx.x == 64, abort_flag);
-        if (valid && ok && half == 0) {
-            const long long gr = row0 + grow;
+            epilogue_tma_store<C::HALF, kOutF32>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo,
+                                                 half * C::HALF, r_begin, pslab, ext, have_o, threadIdx.x == 64,
+                                                 abort_flag, a.status);
+        const long long gr = row0 + grow;
+        const bool row_ok = FMHA_IN_BOUNDS(!valid || (gr >= 0 && gr < a.rows_total && split < (int)gridDim.y),
+                                           kSiteWideLse, a.status);
+        if (valid && ok && row_ok && half == 0) {
             if (!a.to_partials)
                 a.lse[gr] = lse;
             else
                 a.lse_part[(long long)split * a.rows_total + gr] = lse;
         }
-        if (valid && ok && a.to_partials && a.part_f16)
-            a.range_part[((long long)split * a.rows_total + row0 + grow) * 2 + half] = range;
+        if (valid && ok && row_ok && a.to_partials && a.part_f16 &&
+            FMHA_IN_BOUNDS(half == 0 || half == 1, kSiteWideRange, a.status))
+            a.range_part[((long long)split * a.rows_total + gr) * 2 + half] = range;
         tc_fence_before();
     }
     __syncthreads();

@@ -77,7 +77,8 @@ enum fmha_status {
     FMHA_ERR_WORKSPACE = -6,      /* the internal split-KV workspace could not be allocated */
     FMHA_ERR_LAUNCH = -7,         /* a CUDA call failed; the message names it */
     FMHA_ERR_DEVICE_TIMEOUT = -8, /* a kernel's bounded wait gave up (from fmha_check_device_status) */
-    FMHA_ERR_UNSUPPORTED = -9     /* a partial format this shape's kernel does not write */
+    FMHA_ERR_UNSUPPORTED = -9,    /* a partial format this shape's kernel does not write */
+    FMHA_ERR_DEVICE_BOUNDS = -10  /* checked build: a kernel's index check failed (from fmha_check_device_status) */
 };
 
 /*
@@ -197,10 +198,26 @@ int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* l
 size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits);
 
 /* Synchronises `stream`, then reads and clears the current device's status
- * word.  Returns FMHA_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
- * since the last check, FMHA_ERR_LAUNCH if the synchronisation failed, else
- * FMHA_OK. */
+ * word.  Returns FMHA_ERR_DEVICE_BOUNDS if, in a checked build, a kernel's
+ * index check failed since the last check (the message names the check's
+ * site), else FMHA_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up,
+ * FMHA_ERR_LAUNCH if the synchronisation failed, else FMHA_OK. */
 int fmha_check_device_status(fmha_stream_t stream);
+
+/*
+ * Checked build.  The same sources compiled with -DFMHA_CHECKED give
+ * libfmha_gb300_checked.so, with the same entry points.  Its kernels test
+ * every computed shared-memory offset, tensor-memory column, global-memory
+ * index and TMA coordinate against the extent of its buffer before the
+ * access; a failed check skips the access (a warp-collective instruction is
+ * pointed at offset 0 of its buffer instead), and the next
+ * fmha_check_device_status() returns FMHA_ERR_DEVICE_BOUNDS naming the site.
+ * It is a debugging aid and slower; results are otherwise identical.
+ * fmha_build_flags() returns FMHA_BUILD_CHECKED in that library, 0 in the
+ * normal one.
+ */
+#define FMHA_BUILD_CHECKED 1
+int fmha_build_flags(void);
 
 /* Message for the last non-zero return on the calling thread ("" if none). */
 const char* fmha_get_last_error(void);
@@ -219,6 +236,16 @@ void fmha_release(void);
  * hang is involved.
  */
 int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream);
+
+/*
+ * Index-check self-test: launches one thread that runs an index check whose
+ * condition is false, with no memory access behind it.  In the checked build
+ * the next fmha_check_device_status() on this device returns
+ * FMHA_ERR_DEVICE_BOUNDS and names the self-test site; in the normal build
+ * the check is compiled out and nothing is recorded.  Returns FMHA_OK, or
+ * FMHA_ERR_LAUNCH if the launch failed.
+ */
+int fmha_selftest_bounds_check(fmha_stream_t stream);
 
 /*
  * Kernel-family selection for every later call in the process: 0 = automatic
