@@ -49,6 +49,7 @@ SIGNATURES = {
     "fmha_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i32),
     "fmha_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "fmha_build_flags": ([], _i32),
+    "fmha_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "fmha_selftest_bounds_check": ([_vp], _i32),
 }
 # Size of the fixed split-KV scratch fmha_fwd_noalloc uses (FMHA_NOALLOC_SCRATCH_BYTES).
@@ -145,6 +146,34 @@ def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stre
                                   _sink_ptr(sink, n_h), b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
                                   int(bool(causal)), _stream(stream))
         _check(rc, "fmha_fwd_sink")
+    return o, lse
+
+
+def _host(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous host (CPU) %s tensor" % (name, dtype))
+    return t.data_ptr()
+
+
+def fmha_fwd_host(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stream=None):
+    """fmha_fwd on host tensors (fmha_fwd_host): q, k, v are contiguous CPU bf16
+    tensors, preferably page-locked; O and LSE come back in CPU tensors
+    (page-locked ones are allocated if not given).  Stream-ordered: the results
+    are valid, and the inputs may be changed, once `stream` has passed the call."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((b, n_h, T), dtype=torch.float32).pin_memory()
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (b, n_h, T):
+        raise ValueError("o must be [b,n_h,T,hd] and lse [b,n_h,T]")
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd_host(_host(q, "q", torch.bfloat16), _host(k, "k", torch.bfloat16),
+                              _host(v, "v", torch.bfloat16), _host(o, "o", torch.bfloat16),
+                              _host(lse, "lse", torch.float32), b, n_h, n_kv_h, T, s_k, hd, float(scale),
+                              int(window), int(bool(causal)), _stream(stream))
+    _check(rc, "fmha_fwd_host")
     return o, lse
 
 

@@ -13,6 +13,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
 #include <utility>
 
 #include "fmha.h"
@@ -242,14 +243,16 @@ struct Workspace {
     size_t bytes = 0;
 };
 std::mutex g_ws_mu;
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// key: (device, stream, kind); kind 0 = split-KV partials, 1 = fmha_fwd_host's device copies
+std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
+enum WorkspaceKind { kWsPartials = 0, kWsHostIo = 1 };
 
-int workspace(cudaStream_t stream, size_t bytes, void** out) {
+int workspace(cudaStream_t stream, size_t bytes, void** out, int kind = kWsPartials) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     std::lock_guard<std::mutex> lk(g_ws_mu);
-    Workspace& w = g_ws[std::make_pair(dev, stream)];
+    Workspace& w = g_ws[std::make_tuple(dev, stream, kind)];
     if (w.bytes < bytes) {
         if (w.ptr) {
             e = cudaFreeAsync(w.ptr, stream);
@@ -424,6 +427,43 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return fmha_fwd_sink(q, k, v, o, lse, nullptr, batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, stream);
 }
 
+int fmha_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale, int window, int causal,
+                  fmha_stream_t stream) {
+    try {
+        Problem p;
+        int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
+        if (rc) return rc;
+        if (!q_host || ((!k_host || !v_host) && s_k > 0) || !o_host || !lse_host)
+            return fail(FMHA_ERR_NULL, "q, k, v, o and lse must be non-NULL");
+        const long long rows = (long long)batch * n_h * T;
+        if (rows == 0) return FMHA_OK;
+        // device copies, each 256-byte aligned: q | k | v | o | lse
+        auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+        const size_t q_b = (size_t)rows * hd * 2;
+        const size_t kv_b = (size_t)batch * n_kv_h * s_k * hd * 2;
+        const size_t lse_b = (size_t)rows * sizeof(float);
+        const size_t off_k = up(q_b), off_v = off_k + up(kv_b), off_o = off_v + up(kv_b), off_l = off_o + up(q_b);
+        void* ws = nullptr;
+        rc = workspace(stream, off_l + up(lse_b), &ws, kWsHostIo);
+        if (rc) return rc;
+        char* base = static_cast<char*>(ws);
+        cudaError_t e = cudaMemcpyAsync(base, q_host, q_b, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess && kv_b) e = cudaMemcpyAsync(base + off_k, k_host, kv_b, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess && kv_b) e = cudaMemcpyAsync(base + off_v, v_host, kv_b, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+        rc = fmha_fwd(base, base + off_k, base + off_v, base + off_o, reinterpret_cast<float*>(base + off_l), batch,
+                      n_h, n_kv_h, T, s_k, hd, scale, window, causal, stream);
+        if (rc) return rc;
+        e = cudaMemcpyAsync(o_host, base + off_o, q_b, cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, base + off_l, lse_b, cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+        return FMHA_OK;
+    } catch (...) {
+        return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_host");
+    }
+}
+
 int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int window, int causal, int* kv_chunk,
                   int* kernel) {
     Problem p;
@@ -549,7 +589,7 @@ void fmha_release(void) {
     cudaGetDevice(&cur);
     for (auto& kv : g_ws) {
         if (!kv.second.ptr) continue;
-        cudaSetDevice(kv.first.first);
+        cudaSetDevice(std::get<0>(kv.first));
         cudaDeviceSynchronize();
         cudaFree(kv.second.ptr);
     }

@@ -238,6 +238,25 @@ void fmha_release(void);
 int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream);
 
 /*
+ * fmha_fwd from host memory: copies Q, K and V (layouts of fmha_fwd) from
+ * host memory into device buffers the library owns, runs fmha_fwd on them and
+ * copies O (bf16) and LSE (fp32) back into host memory.  Everything is
+ * stream-ordered on `stream` (one cudaMemcpyAsync per tensor, no host
+ * synchronisation), so the host buffers must stay valid and unmodified until
+ * `stream` has passed this call; page-locked host memory gives asynchronous
+ * copies.  The device buffers (Q + K + V + O + LSE bytes) are cached per
+ * device and stream like fmha_fwd's workspace, grown with cudaMallocAsync and
+ * freed by fmha_release(); calls on one stream reuse them in stream order.
+ * Calls on two streams use two sets, so the host-to-device copies of one can
+ * overlap the kernels and the device-to-host copies of the other.
+ * Errors: those of fmha_fwd (host pointers need no alignment), and
+ * FMHA_ERR_WORKSPACE if the device buffers cannot be allocated.
+ */
+int fmha_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                  float scale, int window, int causal, fmha_stream_t stream);
+
+/*
  * Index-check self-test: launches one thread that runs an index check whose
  * condition is false, with no memory access behind it.  In the checked build
  * the next fmha_check_device_status() on this device returns

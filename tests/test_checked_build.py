@@ -78,7 +78,8 @@ def test_checked_build_reports_a_failed_check():
     assert "checked self-test ok" in r.stdout
 
 
-SUITES = ["tests/test_parity.py", "tests/test_kernel_paths.py", "tests/test_sink.py", "tests/test_zz_no_alloc.py"]
+SUITES = ["tests/test_parity.py", "tests/test_kernel_paths.py", "tests/test_sink.py", "tests/test_host_entry.py",
+          "tests/test_zz_no_alloc.py"]
 
 
 @pytest.mark.gpu
