@@ -204,7 +204,11 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         if (lane == 0 && n_tiles > 0) {
             tma_prefetch_desc(&tmv);
             const uint64_t pol = l2_policy_evict_first();
-            for (int j = 0; j < n_tiles; ++j) {
+            // V_0 is needed only after S_0 and its softmax: at hd >= 128, where Q
+            // and K_0 are large, let them take the SM's load bandwidth first
+            // (Q is issued just before K_0; q_full completes once per block).
+            const bool q_in = HD < 128 || mbar_wait(q_full, 0, a.status);
+            for (int j = 0; q_in && j < n_tiles; ++j) {
                 const int s = j % VST;
                 if (j >= VST && !mbar_wait(&v_empty[s], ((j / VST) - 1) & 1, a.status)) break;
                 const int key = k_lo + j * BN;
