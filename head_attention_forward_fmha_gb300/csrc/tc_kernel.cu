@@ -149,6 +149,20 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     const int k_lo = max(c_lo, u_lo), k_hi = min(c_hi, u_hi + 1);
     const int n_tiles = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
 
+    // K tile j into stage j % KST (the caller has made sure the stage is free).
+    uint64_t pol_k = 0;
+    auto issue_k = [&](int j) -> bool {
+        const int s = j % KST;
+        const int key = k_lo + j * BN;
+        if (!FMHA_IN_BOUNDS(key >= 0 && key < k_hi && k_hi <= a.s_k && s < KST, kSiteTcKLoad, a.status)) return false;
+        mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
+#pragma unroll
+        for (int c = 0; c < C::NB; ++c)
+            tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, key, slab, &k_full[s], pol_k);
+        return true;
+    };
+    const int k_first = min(KST, n_tiles);  // K tiles issued before the block barrier
+
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < KST; ++s) {
@@ -166,6 +180,21 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         }
         *abort_flag = 0;
         mbar_fence_init();
+        // Q and the first K stages need no free slot: thread 0, the Q/K
+        // producer, starts them before the block barrier and the TMEM allocation.
+        if (n_tiles > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            pol_k = l2_policy_evict_first();
+            grid_dependency_wait();  // the preceding kernel's writes (Q, K, V) are visible
+            if (FMHA_IN_BOUNDS(r_begin >= 0 && r_begin < a.R && slab < (int)gridDim.z, kSiteTcQLoad, a.status)) {
+                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
+            }
+            for (int j = 0; j < k_first; ++j)
+                if (!issue_k(j)) break;
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -179,24 +208,12 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ Q / K producer
-        if (lane == 0 && n_tiles > 0) {
-            tma_prefetch_desc(&tmq);
-            tma_prefetch_desc(&tmk);
-            if (FMHA_IN_BOUNDS(r_begin >= 0 && r_begin < a.R && slab < (int)gridDim.z, kSiteTcQLoad, a.status)) {
-                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-#pragma unroll
-                for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
-            }
-            const uint64_t pol = l2_policy_evict_first();
-            for (int j = 0; j < n_tiles; ++j) {
+        // Q and K tiles 0 .. k_first-1 went out before the block barrier.
+        if (lane == 0) {
+            for (int j = k_first; j < n_tiles; ++j) {
                 const int s = j % KST;
-                if (j >= KST && !mbar_wait(&k_empty[s], ((j / KST) - 1) & 1, a.status)) break;
-                const int key = k_lo + j * BN;
-                if (!FMHA_IN_BOUNDS(key >= 0 && key < k_hi && k_hi <= a.s_k && s < KST, kSiteTcKLoad, a.status)) break;
-                mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
-#pragma unroll
-                for (int c = 0; c < C::NB; ++c)
-                    tma_load_3d_hint(sk + s * C::KV_TILE + c * BN * 128, &tmk, c * 64, key, slab, &k_full[s], pol);
+                if (!mbar_wait(&k_empty[s], ((j / KST) - 1) & 1, a.status)) break;
+                if (!issue_k(j)) break;
             }
         }
     } else if (warp == 6) {
