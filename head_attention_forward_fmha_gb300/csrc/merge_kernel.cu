@@ -7,7 +7,8 @@
 // One warp per (output row, slice of up to 128 columns): the lanes first
 // share the chunk weights (lane i holds chunk i's weight), then stream the
 // slice of every partial with coalesced 8- or 16-byte loads, several chunks
-// in flight, and write one bf16 slice.  Partials are fp32 (the public
+// in flight, and write one bf16 slice; with at most four chunks every load is
+// issued before any arithmetic.  Partials are fp32 (the public
 // layout) or fp16 (the workspace fmha_fwd uses at hd 512, where partials are a
 // large share of the traffic); an fp16 partial comes with a power-of-two range
 // factor per (chunk, row, 256-column half) that keeps it inside fp16's range.
@@ -64,6 +65,26 @@ __device__ __forceinline__ void load_vec(const __half* p, float (&v)[VEC]) {
     }
 }
 
+// acc * inv -> V bf16 values at dst (RNE).
+template <int V>
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float (&acc)[V], float inv) {
+    if constexpr (V == 8) {
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4*>(dst) = pk;
+    } else if constexpr (V == 4) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
 template <int HD, typename PT, bool SINK>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_lse_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
@@ -85,6 +106,56 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
     constexpr float kLog2e = 1.4426950408889634f;
     constexpr float kLn2 = 0.693147180559945309f;
+
+    // Up to kFast chunks: every load (LSEs, range factors, the partial
+    // slices) is issued before any arithmetic, so the warp waits for one
+    // memory round trip instead of two.
+    constexpr int kFast = 4;
+    if (n_splits <= kFast) {
+        const float lv = (lane < n_splits) ? __ldg(lse_parts + (long long)lane * rows + row) : -INFINITY;
+        float rv = 1.f;
+        if constexpr (sizeof(PT) == 2) {
+            if (lane < n_splits && FMHA_IN_BOUNDS(col / 256 < 2, kSiteMergeRange, status))
+                rv = __ldg(range_parts + ((long long)lane * rows + row) * 2 + col / 256);
+        }
+        float pv[kFast][V];
+#pragma unroll
+        for (int i = 0; i < kFast; ++i) {
+            if (i < n_splits) {
+                load_vec<V>(o_parts + ((long long)i * rows + row) * HD + col, pv[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) pv[i][e] = 0.f;
+            }
+        }
+        float m = lv;
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sft));
+        const int head = (int)((row / T) % n_h);
+        const float sg = (SINK && FMHA_IN_BOUNDS(head >= 0 && head < n_h, kSiteMergeSink, status))
+                             ? __ldg(sink + head)
+                             : -INFINITY;
+        m = fmaxf(m, sg);
+        const float w_den = (m != -INFINITY && lane < n_splits) ? exp2f((lv - m) * kLog2e) : 0.f;
+        const float w_mine = w_den * rv;
+        float den = w_den;
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) den += __shfl_xor_sync(0xffffffffu, den, sft);
+        if (SINK && sg != -INFINITY) den += exp2f((sg - m) * kLog2e);
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < kFast; ++i) {
+            const float wi = __shfl_sync(0xffffffffu, w_mine, i);  // 0 past n_splits
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] += wi * pv[i][e];
+        }
+        const float inv = (den > 0.f) ? 1.f / den : 0.f;
+        store_row<V>(o + row * HD + col, acc, inv);
+        if (lane == 0 && col == 0) lse[row] = (den > 0.f) ? m + log2f(den) * kLn2 : -INFINITY;
+        return;
+    }
 
     float mx = -INFINITY;
     for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, __ldg(lse_parts + (long long)i * rows + row));
@@ -142,22 +213,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
     if (SINK && sg != -INFINITY) den += exp2f((sg - mx) * kLog2e);
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
-    __nv_bfloat16* dst = o + row * HD + col;
-    if constexpr (V == 8) {
-        uint4 pk;
-        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-        pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(dst) = pk;
-    } else if constexpr (V == 4) {
-        uint2 pk;
-        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(dst) = pk;
-    } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
+    store_row<V>(o + row * HD + col, acc, inv);
     if (lane == 0 && col == 0) lse[row] = (den > 0.f) ? mx + log2f(den) * kLn2 : -INFINITY;
 }
 
