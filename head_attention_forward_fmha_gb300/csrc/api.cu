@@ -5,6 +5,7 @@
 // synchronises the host except fmha_check_device_status() and fmha_release().
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -110,6 +111,16 @@ int check_inputs(const void* q, const void* k, const void* v, int s_k) {
     if (!q || ((!k || !v) && s_k > 0)) return fail(FMHA_ERR_NULL, "q, k and v must be non-NULL");
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
         return fail(FMHA_ERR_ALIGN, "q, k and v must be 16-byte aligned");
+    return FMHA_OK;
+}
+
+// Chunk count limits: the grid's y dimension, and partial slabs addressed as
+// split * (batch * n_kv_h) + slab by 32-bit TMA coordinates.
+int check_chunks(const Problem& p, int n_splits) {
+    if (n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks (%d)", n_splits);
+    if ((long long)n_splits * p.batch * p.n_kv_h > INT_MAX)
+        return fail(FMHA_ERR_SHAPE, "KV chunks x batch x n_kv_h = %lld exceeds 2^31 - 1",
+                    (long long)n_splits * p.batch * p.n_kv_h);
     return FMHA_OK;
 }
 
@@ -403,7 +414,8 @@ int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* l
         const long long rows = (long long)batch * n_h * T;
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = choose_split(p);
-        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
+        rc = check_chunks(p, sp.n_splits);
+        if (rc) return rc;
         if (sp.n_splits == 1)
             return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream, false, nullptr, sink);
         void* ws = nullptr;
@@ -509,7 +521,8 @@ int fmha_fwd_splitkv_ex(const void* q, const void* k, const void* v, void* o_par
         const long long rows = (long long)batch * n_h * T;
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = split_layout(T, s_k, window, kv_chunk);
-        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks (%d)", sp.n_splits);
+        rc = check_chunks(p, sp.n_splits);
+        if (rc) return rc;
         return run_kernel(q, k, v, p, sp, nullptr, nullptr, o_parts, lse_parts, true, stream, f16,
                           f16 ? range_parts : nullptr);
     } catch (...) {
@@ -668,7 +681,8 @@ extern "C" int fmha_fwd_noalloc(const void* q, const void* k, const void* v, voi
         const long long rows = (long long)batch * n_h * T;
         if (rows == 0) return FMHA_OK;
         const SplitPlan sp = choose_split(p);
-        if (sp.n_splits > 65535) return fail(FMHA_ERR_SHAPE, "too many KV chunks");
+        rc = check_chunks(p, sp.n_splits);
+        if (rc) return rc;
         if (sp.n_splits == 1) return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
         const size_t need = partial_bytes(rows, hd, sp.n_splits);
         if (need > (size_t)FMHA_NOALLOC_SCRATCH_BYTES)

@@ -107,6 +107,11 @@ def test_splitkv_and_merge_argument_errors(lib):
     assert m(16, 16, 2, 24, 16, 1, 1, 1, 64, None) == -2
     assert m(16, 16, 2, 16, 16, 0, 1, 1, 64, None) == 0                            # empty
     assert lib.fmha_split_layout(1, 10, 0, 0, None) == -5
+    # chunk count limits: more than 65535 chunks, and chunks x batch x n_kv_h past 2^31 - 1
+    assert f(16, 16, 16, 16, 16, 1, 1, 1, 1, 1, 70000, 64, 0.1, 0, 0, None) == -5
+    assert "too many KV chunks" in binding.fmha_get_last_error()
+    assert f(16, 16, 16, 16, 16, 1, 40000, 1, 1, 1, 60000, 64, 0.1, 0, 0, None) == -5
+    assert "exceeds 2^31 - 1" in binding.fmha_get_last_error()
 
 
 def test_f16_partials_only_on_the_hd512_tensor_core_kernel(lib):
