@@ -223,7 +223,6 @@ cudaError_t launch_t(const PT* o_parts, const float* lse_parts, const float* ran
                      unsigned* status) {
     const long long tasks = rows * MCfg<HD, PT>::NSLICE;
     const long long blocks = (tasks + kMergeWarps - 1) / kMergeWarps;
-    if (blocks > 2147483647LL) return cudaErrorInvalidConfiguration;  // grid x limit
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kMergeWarps * 32);
