@@ -92,6 +92,8 @@ int check_shape(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float sc
     if ((long long)batch * n_kv_h > 65535)
         return fail(FMHA_ERR_SHAPE, "batch * n_kv_h = %lld exceeds 65535", (long long)batch * n_kv_h);
     if ((long long)n_h / n_kv_h * T > (1LL << 30)) return fail(FMHA_ERR_SHAPE, "too many query rows per KV head");
+    if ((long long)batch * n_h * T > INT_MAX)  // also bounds the merge grid (one block per 8 row slices)
+        return fail(FMHA_ERR_SHAPE, "batch * n_h * T = %lld query rows exceeds 2^31 - 1", (long long)batch * n_h * T);
     out->batch = batch;
     out->n_h = n_h;
     out->n_kv_h = n_kv_h;

@@ -112,6 +112,8 @@ def test_splitkv_and_merge_argument_errors(lib):
     assert "too many KV chunks" in binding.fmha_get_last_error()
     assert f(16, 16, 16, 16, 16, 1, 40000, 1, 1, 1, 60000, 64, 0.1, 0, 0, None) == -5
     assert "exceeds 2^31 - 1" in binding.fmha_get_last_error()
+    assert lib.fmha_fwd(16, 16, 16, 16, 16, 60000, 1024, 1, 64, 64, 64, 0.1, 0, 0, None) == -5   # 3.9e9 rows
+    assert "query rows exceeds" in binding.fmha_get_last_error()
 
 
 def test_f16_partials_only_on_the_hd512_tensor_core_kernel(lib):
