@@ -205,7 +205,9 @@ size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_spl
 int fmha_check_device_status(fmha_stream_t stream);
 
 /*
- * Checked build.  The same sources compiled with -DFMHA_CHECKED give
+ * Checked build (no counterpart on the pages; the pages debugged an illegal
+ * memory access by hand, CURRENT_ISSUE.md "Key lessons from this session").
+ * The same sources compiled with -DFMHA_CHECKED give
  * libfmha_gb300_checked.so, with the same entry points.  Its kernels test
  * every computed shared-memory offset, tensor-memory column, global-memory
  * index and TMA coordinate against the extent of its buffer before the
@@ -238,6 +240,8 @@ void fmha_release(void);
 int fmha_selftest_wait_timeout(unsigned timeout_us, fmha_stream_t stream);
 
 /*
+ * (This entry point has no counterpart on the pages the method comes from;
+ * the computation is fmha_fwd's.)
  * fmha_fwd from host memory: copies Q, K and V (layouts of fmha_fwd) from
  * host memory into device buffers the library owns, runs fmha_fwd on them and
  * copies O (bf16) and LSE (fp32) back into host memory.  Everything is
