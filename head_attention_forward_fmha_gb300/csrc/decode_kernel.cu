@@ -20,6 +20,7 @@
 // chunk for the LSE merge (CURRENT_ISSUE.md, "Next steps" item 4).
 #include <cfloat>
 #include <climits>
+#include <atomic>
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
             for (int it = 0; it < n_tiles; ++it) {
                 const int s = it % C::STAGES;
                 if (it >= C::STAGES && !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, a.status)) break;
@@ -139,7 +141,11 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
                     tma_load_3d_hint(kst + c * C::BOX_BYTES, &tmk, c * 64, key, slab, &full[s], pol);
                     tma_load_3d_hint(vst + c * C::BOX_BYTES, &tmv, c * 64, key, slab, &full[s], pol);
                 }
+                ++issued;
             }
+            // Exit drain: the stages this warp loaded have landed before the
+            // block may exit, even if the consumers gave up on their waits.
+            drain_ring(full, C::STAGES, issued, a.status);
         }
         return;
     }
@@ -385,7 +391,7 @@ template <int HD, int NB, bool SINK>
 cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     using C = DCfg<HD, NB>;
     auto kern = decode_splitkv_kernel<HD, NB, SINK>;
-    static bool attr_set[128] = {};
+    static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

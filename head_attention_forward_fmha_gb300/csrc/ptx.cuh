@@ -149,6 +149,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
     }
 }
 
+// Exit drain of a producer thread.  `issued` loads went into a ring of `nslots`
+// slots, load i into slot i % nslots, each completing one phase of full[slot].
+// Waits (bounded, as mbar_wait) until the last load issued into every slot has
+// landed -- slot s last received load s + ((issued - 1 - s) / nslots) * nslots,
+// whose phase has that index / nslots -- so that no TMA write into this
+// block's shared memory is still in flight when the block exits, whether or
+// not a consumer gave up on its waits.  Nothing arms these barriers after
+// the producer stops, so each waited-for phase is the barrier's latest.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int nslots, int issued, unsigned* status) {
+    for (int s = 0; s < nslots && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / nslots) * nslots;
+        mbar_wait(&full[s], (unsigned)(last / nslots) & 1u, status);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tensor) loads into shared memory, completing on an mbarrier
 // ---------------------------------------------------------------------------
@@ -237,6 +252,34 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Packed fp32 pairs (sm_100 and later): two lanes of fp32 arithmetic in one
+// instruction, on a 64-bit register holding {lo, hi}.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The two bf16 halves of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t pk) { return __uint_as_float(pk << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pk) { return __uint_as_float(pk & 0xffff0000u); }
+
 // 2^x with the hardware approximation (ex2.approx.ftz.f32: ~2 ulp, -inf -> 0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -251,23 +294,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //   M = max(m, sink), l' = l 2^(m - M) + 2^(sink - M), inv = 2^(m - M) / l',
 //   lse = (M + log2 l') ln 2.
 // No attended key gives O = 0 and lse = sink (-inf without one).
-__device__ __forceinline__ void finish_row(float m, float l, float sink_l2, float& inv, float& lse) {
+//
+// l_o: the divisor of O, when it differs from l.  A kernel that rounds P to
+// bf16 before the P V product divides O by the sum of the ROUNDED values
+// (the weights it actually multiplied V by), so that O is an exact convex
+// combination of V rows whatever the rounding -- a dominant key's V row comes
+// back unchanged -- while the LSE keeps the sum of the unrounded
+// probabilities.  Both sums are relative to the same m.
+__device__ __forceinline__ void finish_row(float m, float l, float l_o, float sink_l2, float& inv, float& lse) {
     constexpr float kLn2 = 0.693147180559945309f;
-    if (!(l > 0.f)) {
+    if (!(l > 0.f) || !(l_o > 0.f)) {
         inv = 0.f;
         lse = sink_l2 * kLn2;
         return;
     }
     if (sink_l2 == -INFINITY) {
-        inv = 1.f / l;
+        inv = 1.f / l_o;
         lse = (m + log2f(l)) * kLn2;
         return;
     }
     const float M = fmaxf(m, sink_l2);
     const float c = exp2f(m - M);
-    const float lt = l * c + exp2f(sink_l2 - M);
-    inv = c / lt;
-    lse = (M + log2f(lt)) * kLn2;
+    const float ls = exp2f(sink_l2 - M);
+    inv = c / (l_o * c + ls);
+    lse = (M + log2f(l * c + ls)) * kLn2;
+}
+
+__device__ __forceinline__ void finish_row(float m, float l, float sink_l2, float& inv, float& lse) {
+    finish_row(m, l, l, sink_l2, inv, lse);
 }
 
 // Query head h's sink logit in log2 units.  The kernels take the sink as a

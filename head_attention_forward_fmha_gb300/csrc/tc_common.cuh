@@ -6,16 +6,20 @@
 
 namespace fmha {
 
-// One row's S tile (raw dot products, x[BN]) -> un-normalised probabilities
-// in place, updating the running reference max m_ref and sum l (FA2 online
-// softmax: commit e4ee9fd of the nvfp4-megamoe-kernel pages, multi-tile C API
-// part).  Keys outside [jlo, jhi] are masked.  sl2 = scale * log2(e).
-// The reference max only moves when the tile's max exceeds it by more than
-// 8 (log2 units); then alpha = 2^(m_old - m_new) and the caller rescales O.
-// Probabilities are therefore <= 2^8.
+// One row's S tile (raw dot products, x[BN]) -> un-normalised probabilities,
+// written as packed bf16 pairs to p[BN / 2] (key 2i in the low half), while
+// the running reference max m_ref and two running sums are updated (FA2
+// online softmax: commit e4ee9fd of the nvfp4-megamoe-kernel pages,
+// multi-tile C API part): l sums the fp32 probabilities (it gives the LSE),
+// l_o the bf16-rounded ones that the P V product multiplies V by (O is
+// divided by it, see finish_row).  Keys outside [jlo, jhi] are masked.
+// sl2 = scale * log2(e).  The reference max only moves when the tile's max
+// exceeds it by more than 8 (log2 units); then alpha = 2^(m_old - m_new) and
+// the caller rescales O.  Probabilities are therefore <= 2^8.  The
+// scale-and-subtract and both sums run on packed fp32 pairs.
 template <int BN>
-__device__ __forceinline__ void softmax_row_tile(float (&x)[BN], int key0, int jlo, int jhi, float sl2, float& m_ref,
-                                                 float& l, float& alpha) {
+__device__ __forceinline__ void softmax_row_tile(float (&x)[BN], uint32_t (&p)[BN / 2], int key0, int jlo, int jhi,
+                                                 float sl2, float& m_ref, float& l, float& l_o, float& alpha) {
     const bool full = key0 >= jlo && key0 + BN - 1 <= jhi;
     float mt, mul;
     if (sl2 > 0.f) {
@@ -53,21 +57,34 @@ __device__ __forceinline__ void softmax_row_tile(float (&x)[BN], int key0, int j
         alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
     }
     const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint64_t mul2 = f32x2(mul, mul), nmu2 = f32x2(-mu, -mu);
+    uint64_t s2[2] = {0ull, 0ull}, r2[2] = {0ull, 0ull};  // {even, odd} key sums, two chains each
 #pragma unroll
-    for (int i = 0; i < BN; ++i) {
-        x[i] = ex2_approx(fmaf(x[i], mul, -mu));  // masked keys: 2^-inf = 0
-        s4[i & 3] += x[i];
+    for (int i = 0; i < BN / 2; ++i) {
+        float y0, y1;
+        f32x2_split(fma_f32x2(f32x2(x[2 * i], x[2 * i + 1]), mul2, nmu2), y0, y1);
+        y0 = ex2_approx(y0);  // masked keys: 2^-inf = 0
+        y1 = ex2_approx(y1);
+        const uint32_t pk = pack_bf16x2(y0, y1);
+        p[i] = pk;
+        s2[i & 1] = add_f32x2(s2[i & 1], f32x2(y0, y1));
+        r2[i & 1] = add_f32x2(r2[i & 1], f32x2(bf16_lo(pk), bf16_hi(pk)));
     }
-    l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+    float a0, a1, b0, b1, c0, c1, d0, d1;
+    f32x2_split(s2[0], a0, a1);
+    f32x2_split(s2[1], b0, b1);
+    f32x2_split(r2[0], c0, c1);
+    f32x2_split(r2[1], d0, d1);
+    l = l * alpha + ((a0 + a1) + (b0 + b1));
+    l_o = l_o * alpha + ((c0 + c1) + (d0 + d1));
     m_ref = m_new;
 }
 
-// Row `row` of P (BN bf16 values) into the A-operand layout: groups of 64 keys,
-// each a 128-row x 128-byte K-major tile with the 128-byte swizzle (16-byte
-// chunk c of row r stored at chunk c ^ (r % 8)).
+// Row `row` of P (BN bf16 values, packed in pairs) into the A-operand layout:
+// groups of 64 keys, each a 128-row x 128-byte K-major tile with the 128-byte
+// swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)).
 template <int BN>
-__device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float (&x)[BN]) {
+__device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const uint32_t (&p)[BN / 2]) {
     constexpr int GROUPS = (BN + 63) / 64;
     constexpr int CHUNKS = (BN < 64 ? BN : 64) / 8;
 #pragma unroll
@@ -75,12 +92,8 @@ __device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float 
         uint8_t* prow = pbuf + g * 128 * 128 + row * 128;
 #pragma unroll
         for (int ch = 0; ch < CHUNKS; ++ch) {
-            const float* pv = x + g * 64 + ch * 8;
-            uint4 pk;
-            pk.x = pack_bf16x2(pv[0], pv[1]);
-            pk.y = pack_bf16x2(pv[2], pv[3]);
-            pk.z = pack_bf16x2(pv[4], pv[5]);
-            pk.w = pack_bf16x2(pv[6], pv[7]);
+            const uint32_t* pv = p + g * 32 + ch * 4;
+            const uint4 pk = make_uint4(pv[0], pv[1], pv[2], pv[3]);
             *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
         }
     }

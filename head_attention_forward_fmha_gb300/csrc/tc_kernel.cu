@@ -31,6 +31,7 @@
 // warp-collective: the TMEM epilogue hang on the 593bc25 page), and TMEM is
 // released with the address tcgen05.alloc returned.
 #include <climits>
+#include <atomic>
 #include "internal.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -59,7 +60,7 @@ struct TCfg {
     static constexpr int OFF_V = OFF_K + KST * KV_TILE;
     static constexpr int OFF_P = OFF_V + VST * KV_TILE;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2;
+    static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1;
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HD <= TMEM_COLS, "S double buffer + O must fit in TMEM");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     uint64_t* s_full = v_empty + VST;  // [2] by S buffer
     uint64_t* p_ready = s_full + 2;    // [2] by P buffer
     uint64_t* o_done = p_ready + 2;    // [2] by P buffer: PV of a tile using that P buffer completed
+    uint64_t* mma_drain = o_done + 2;  // every MMA the issuer launched has completed (exit drain)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -162,6 +164,8 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         return true;
     };
     const int k_first = min(KST, n_tiles);  // K tiles issued before the block barrier
+    int k_issued = 0;                        // thread 0: K tiles issued (0 .. k_issued-1)
+    bool q_issued = false;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             mbar_init(&p_ready[b2], 128);
             mbar_init(&o_done[b2], 1);
         }
+        mbar_init(mma_drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
         // Q and the first K stages need no free slot: thread 0, the Q/K
@@ -191,9 +196,12 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c) tma_load_3d(sq + c * BM * 128, &tmq, c * 64, r_begin, slab, q_full);
+                q_issued = true;
             }
-            for (int j = 0; j < k_first; ++j)
+            for (int j = 0; j < k_first; ++j) {
                 if (!issue_k(j)) break;
+                ++k_issued;
+            }
         }
     }
     if (warp == 1) {
@@ -210,11 +218,14 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         // ------------------------------------------------------------ Q / K producer
         // Q and K tiles 0 .. k_first-1 went out before the block barrier.
         if (lane == 0) {
-            for (int j = k_first; j < n_tiles; ++j) {
+            for (int j = k_first; k_issued == j && j < n_tiles; ++j) {
                 const int s = j % KST;
                 if (!mbar_wait(&k_empty[s], ((j / KST) - 1) & 1, a.status)) break;
                 if (!issue_k(j)) break;
+                ++k_issued;
             }
+            drain_ring(k_full, KST, k_issued, a.status);
+            if (q_issued) mbar_wait(q_full, 0, a.status);
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ V producer
@@ -225,6 +236,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             // and K_0 are large, let them take the SM's load bandwidth first
             // (Q is issued just before K_0; q_full completes once per block).
             const bool q_in = HD < 128 || mbar_wait(q_full, 0, a.status);
+            int v_issued = 0;
             for (int j = 0; q_in && j < n_tiles; ++j) {
                 const int s = j % VST;
                 if (j >= VST && !mbar_wait(&v_empty[s], ((j / VST) - 1) & 1, a.status)) break;
@@ -234,7 +246,9 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < C::NB; ++c)
                     tma_load_3d_hint(sv + s * C::KV_TILE + c * BN * 128, &tmv, c * 64, key, slab, &v_full[s], pol);
+                ++v_issued;
             }
+            drain_ring(v_full, VST, v_issued, a.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -282,6 +296,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 tc_commit(&v_empty[s]);
                 if (j + 2 < n_tiles && !issue_qk(j + 2)) break;
             }
+            // Exit drain: whatever the loop issued has completed before TMEM
+            // and the operand buffers are released, even if a wait gave up.
+            tc_commit(mma_drain);
+            mbar_wait(mma_drain, 0, a.status);
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
@@ -296,7 +314,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             jlo = max(jlo, c_lo);
             jhi = min(jhi, c_hi - 1);
         }
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int pb = j & 1;
@@ -319,7 +337,8 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             tmem_wait_ld();
             // Exponentials and the row sum before waiting on the tensor core.
             float alpha;
-            softmax_row_tile<BN>(x, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, alpha);
+            uint32_t pk[BN / 2];
+            softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
             // P buffer pb was last read by PV_{j-2}; a rescale of O needs PV_{j-1} done.
             if (rescale) {
@@ -334,7 +353,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 }
             }
             if (FMHA_IN_BOUNDS(row >= 0 && row < BM && pb < 2, kSiteTcPRow, a.status))
-                write_p_row<BN>(sp + pb * C::P_BYTES, row, x);
+                write_p_row<BN>(sp + pb * C::P_BYTES, row, pk);
             if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         tc_fence_after();
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
-        finish_row(m_ref, l,
+        finish_row(m_ref, l, l_o,
                    (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T, a.n_h, a.status) : -INFINITY,
                    inv, lse);
         // O -> shared memory (the drained K/V stages) -> TMA store; rows past
@@ -397,7 +416,7 @@ template <int HD, bool SINK>
 cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     using C = TCfg<HD>;
     auto kern = fwd_tc_kernel<HD, SINK>;
-    static bool attr_set[128] = {};
+    static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

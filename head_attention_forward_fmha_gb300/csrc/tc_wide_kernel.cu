@@ -14,6 +14,7 @@
 // halves compute identical (max, sum), and half 0 writes the LSE.
 #include <algorithm>
 #include <climits>
+#include <atomic>
 #include "internal.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -51,7 +52,7 @@ struct WCfgT {
     static constexpr int OFF_P = OFF_RING + NSLOT * SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
     static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging (128 KB)
-    static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + (QRES ? 1 : 0);
+    static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + 1 + (QRES ? 1 : 0);
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     uint64_t* s_full = slot_empty + C::NSLOT;  // [2]
     uint64_t* p_ready = s_full + 2;
     uint64_t* o_done = p_ready + 1;
-    uint64_t* q_full = o_done + 1;  // QRES only
+    uint64_t* mma_drain = o_done + 1;  // every MMA the issuer launched has completed (exit drain)
+    uint64_t* q_full = mma_drain + 1;  // QRES only
     uint8_t* qres = smem + C::OFF_Q;
     uint8_t* stage = smem + C::OFF_STAGE;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
@@ -160,7 +162,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         }
     };
     uint64_t pol_kv = 0, pol_q = 0;
-    auto issue_item = [&](int i) {
+    int issued = 0;  // thread 0: items issued (0 .. issued-1)
+    bool q_issued = false;
+    auto issue_item = [&](int i) -> bool {
         int kind, tile, c;
         item_of(i, kind, tile, c);
         const int s = i % C::NSLOT;
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                             : kind == 1 ? (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::Q_CHUNKS)
                                         : (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::V_ITEMS);
         if (!FMHA_IN_BOUNDS(in_range && s >= 0 && s < C::NSLOT && slab < (int)gridDim.z, kSiteWideItem, a.status))
-            return;
+            return false;
         mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
         uint8_t* dst = ring + s * C::SLOT_BYTES;
         if (kind == 0)
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             tma_load_3d_hint(dst, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
         else
             tma_load_3d_hint(dst, &tmv, half * C::HALF + c * 64, key, slab, &slot_full[s], pol_kv);
+        return true;
     };
 
     if (threadIdx.x == 0) {
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         mbar_init(&s_full[1], 1);
         mbar_init(p_ready, 128);
         mbar_init(o_done, 1);
+        mbar_init(mma_drain, 1);
         if (QRES) mbar_init(q_full, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -205,8 +211,12 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 mbar_arrive_expect_tx(q_full, C::Q_CHUNKS * C::SLOT_BYTES);
                 for (int c = 0; c < C::Q_CHUNKS; ++c)
                     tma_load_3d_hint(qres + c * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, q_full, pol_q);
+                q_issued = true;
             }
-            for (int i = 0; i < min(C::NSLOT, n_items); ++i) issue_item(i);
+            for (int i = 0; i < min(C::NSLOT, n_items); ++i) {
+                if (!issue_item(i)) break;
+                ++issued;
+            }
         }
     }
     if (warp == 1) {
@@ -223,11 +233,14 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         // ------------------------------------------------------------ producer
         // Items 0 .. NSLOT-1 went out before the block barrier.
         if (lane == 0) {
-            for (int i = C::NSLOT; i < n_items; ++i) {
+            for (int i = C::NSLOT; issued == i && i < n_items; ++i) {
                 const int s = i % C::NSLOT;
                 if (!mbar_wait(&slot_empty[s], ((i / C::NSLOT) - 1) & 1, a.status)) break;
-                issue_item(i);
+                if (!issue_item(i)) break;
+                ++issued;
             }
+            drain_ring(slot_full, C::NSLOT, issued, a.status);
+            if (q_issued) mbar_wait(q_full, 0, a.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -293,6 +306,10 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 for (int c = 0; c < C::V_ITEMS; ++c) tc_commit(&slot_empty[sv0 + c]);
                 tc_commit(o_done);
             }
+            // Exit drain: whatever the loop issued has completed before TMEM
+            // and the operand buffers are released, even if a wait gave up.
+            tc_commit(mma_drain);
+            mbar_wait(mma_drain, 0, a.status);
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
@@ -307,7 +324,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             jlo = max(jlo, c_lo);
             jhi = min(jhi, c_hi - 1);
         }
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status)) {
@@ -327,13 +344,14 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             }
             tmem_wait_ld();
             float alpha;
-            softmax_row_tile<BN>(x, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, alpha);
+            uint32_t pk[BN / 2];
+            softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
             // PV_{j-1} must be complete before P is overwritten and O rescaled.
             if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
                 ok = false;
                 break;
             }
-            if (FMHA_IN_BOUNDS(row >= 0 && row < BM, kSiteWidePRow, a.status)) write_p_row<BN>(sp, row, x);
+            if (FMHA_IN_BOUNDS(row >= 0 && row < BM, kSiteWidePRow, a.status)) write_p_row<BN>(sp, row, pk);
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 tc_fence_after();
 #pragma unroll 1
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         tc_fence_after();
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
-        finish_row(m_ref, l,
+        finish_row(m_ref, l, l_o,
                    (SINK && valid) ? sink_log2_of(a.sink, kvh * a.group + grow / a.T, a.n_h, a.status) : -INFINITY,
                    inv, lse);
         const bool have_o = ok && n_tiles > 0;
@@ -435,7 +453,7 @@ int tc_wide_kv_tile() { return WCfg::BN; }
 template <bool SINK, bool QRES>
 cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     using C = WCfgT<QRES>;
-    static bool attr_set[128] = {};
+    static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -151,17 +151,38 @@ def test_merge_kernel_against_oracle(hd):
 SWEEP = inputs.sweep()
 
 
+def _sweep_slabs(w, n, seed):
+    """n distinct (batch, head) pairs: the first, the last and seeded others."""
+    rng = np.random.default_rng(seed)
+    pairs = [(0, 0), (w.batch - 1, w.n_h - 1)]
+    while len(pairs) < n:
+        p = (int(rng.integers(w.batch)), int(rng.integers(w.n_h)))
+        if p not in pairs:
+            pairs.append(p)
+    return pairs
+
+
 @pytest.mark.parametrize("w", SWEEP, ids=[w.name for w in SWEEP])
 def test_sweep_full_size_sampled_rows(w):
+    """Full-size run; the oracle recomputes 48 sampled rows plus every row of
+    four whole (batch, head) slabs, so that all three tolerances -- max |dO|,
+    |dLSE| and the per-(batch, head) cosine over the T x hd block -- are
+    asserted at every point of the sweep."""
     qd, kd, vd = inputs.make_inputs(w, seed=5, device="cuda")
     o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale)
     torch.cuda.synchronize()
     binding.fmha_check_device_status()
-    rows = inputs.sample_rows(w, 48, seed=5)
+    slabs = _sweep_slabs(w, 4, seed=5)
+    slab_rows = np.concatenate([(b * w.n_h + h) * w.T + np.arange(w.T, dtype=np.int64) for b, h in slabs])
+    rows = np.union1d(inputs.sample_rows(w, 48, seed=5), slab_rows)
     o_ref, lse_ref = oracle.attention_rows(to_np_bits(qd), to_np_bits(kd), to_np_bits(vd), rows, w.scale)
-    og = o.reshape(-1, w.hd)[torch.from_numpy(rows).cuda()]
-    lg = lse.reshape(-1)[torch.from_numpy(rows).cuda()]
+    idx = torch.from_numpy(rows).cuda()
+    og = o.reshape(-1, w.hd)[idx]
+    lg = lse.reshape(-1)[idx]
     compare(og, lg, o_ref, lse_ref, w.name)
+    pos = np.searchsorted(rows, slab_rows)
+    og_slabs = og[torch.from_numpy(pos).cuda()].reshape(1, len(slabs), w.T, w.hd)
+    cosine_per_head(og_slabs, o_ref[pos].reshape(1, len(slabs), w.T, w.hd), w.name)
     del qd, kd, vd, o, lse
     torch.cuda.empty_cache()
 
