@@ -19,8 +19,9 @@ host buffers, ``fmha_fwd_host``: per step the H2D copies of Q, K, V from
 page-locked memory, the forward, and the D2H copies of O and LSE; steps
 alternate between two streams), ``clocks``
 (nvidia-smi sampled during the timed region), ``gpu_launches`` and
-``secondary`` (the GQA sliding-window decode, and the causal prefill, each with
-its own roofline figures, as ``fmha_fwd`` plans them; for the GQA decode also
+``secondary`` (the single-head decode -- launch-latency bound, read its
+``us_per_step`` --, the GQA sliding-window decode and the causal prefill, each
+with its own roofline figures, as ``fmha_fwd`` plans them; for the GQA decode also
 ``split_512``: the same workload split literally into 512-key chunks with
 ``fmha_fwd_splitkv`` + ``fmha_merge``).
 
@@ -416,7 +417,8 @@ def run_e2e(binding, w, steps, stream):
         binding.fmha_fwd_host(q, k, v, o, lse, scale=w.scale, window=w.window, causal=w.causal,
                               stream=streams[i % 2])
 
-    for i in range(4):
+    # Every host set (on both streams) makes its first DMA here, not in the timed region.
+    for i in range(2 * n_sets + 2):
         step(i)
     torch.cuda.synchronize()
     e0, e1, e_side = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -434,6 +436,26 @@ def run_e2e(binding, w, steps, stream):
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = outs[0][0].numel() * 2 + outs[0][1].numel() * 4
     return ms, h2d, d2h
+
+
+def h2d_link_gbs(stream, nbytes):
+    """Host-to-device bandwidth of one page-locked copy of `nbytes` (about one
+    step's inputs), best of 10, measured in the same run as the e2e figure: the
+    ceiling the e2e step time is set against."""
+    nbytes = max(1 << 20, int(nbytes))
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        dst.copy_(src, non_blocking=True)
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+    return nbytes / (best * 1e-3) / 1e9
 
 
 def cpu_baseline(w, budget_s=15.0):
@@ -550,12 +572,14 @@ def main():
     time.sleep(0.3)
     res = run_workload(binding, w, args.steps, args.warmup, stream, dist)
     clocks = sampler.summary(res["t0"], res["t1"])
-    e2e_ms, h2d, d2h = run_e2e(binding, w, max(10, min(args.steps, 200)), stream)
+    e2e_steps = max(200, min(args.steps, 2000))
+    e2e_ms, h2d, d2h = run_e2e(binding, w, e2e_steps, stream)
     e2e_ms = max_over_ranks(e2e_ms, dist)
+    link_gbs = h2d_link_gbs(stream, h2d)
 
     secondary = {}
     if not args.no_secondary:
-        for name, chunk in (("gqa_swa_decode", 512), ("causal_prefill", 0)):
+        for name, chunk in (("single_head_decode", 0), ("gqa_swa_decode", 512), ("causal_prefill", 0)):
             w2 = inputs.WORKLOADS[name]
             st = max(20, min(args.steps, 400))
             r2 = run_workload(binding, w2, st, 3, stream, dist)
@@ -572,6 +596,7 @@ def main():
                 "kernel_ms": round(r2["decode_ms"], 5), "merge_kernel_ms": round(r2["merge_ms"], 5),
                 "traffic": recorded_traffic(r2["kernel"], name),
                 "steps": st,
+                "us_per_step": round(r2["ms_per_step"] * 1e3, 3),
             }
             if chunk:
                 ms_c, n_c = run_explicit_split(binding, w2, chunk, st, stream)
@@ -601,7 +626,9 @@ def main():
         "kernels_ms": {res["kernel"]: round(res["decode_ms"], 6), "merge_lse": round(res["merge_ms"], 6)},
         "tflops": round(algo_flops(w) / (res["ms_per_step"] * 1e-3) / 1e12, 2),
         "e2e": {"value": round(bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_link_gbs": round(link_gbs, 1),
+                "h2d_floor_ms": round(h2d / (link_gbs * 1e9) * 1e3, 4)},
         "gpu_launches": args.steps * res["launches_per_step"],
         "clocks": clocks,
         "secondary": secondary,

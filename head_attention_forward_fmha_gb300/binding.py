@@ -41,6 +41,7 @@ SIGNATURES = {
     "fmha_merge_ex": ([_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "fmha_fwd_sink": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "fmha_splitkv_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32], _sz),
+    "fmha_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32], _sz),
     "fmha_check_device_status": ([_vp], _i32),
     "fmha_get_last_error": ([], ctypes.c_char_p),
     "fmha_release": ([], None),
@@ -118,6 +119,18 @@ def _shapes(q, k, v):
     return b, n_h, n_kv_h, T, s_k, hd
 
 
+def _check_outputs(q, o, lse):
+    """o must be shaped like q and lse [b, n_h, T], both on q's device, so that
+    the kernels never write past the end of a caller's buffer."""
+    b, n_h, T, _ = q.shape
+    if not isinstance(o, torch.Tensor) or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must be shaped like q %s" % (tuple(q.shape),))
+    if not isinstance(lse, torch.Tensor) or tuple(lse.shape) != (b, n_h, T):
+        raise ValueError("lse must be [b,n_h,T] = %s" % ((b, n_h, T),))
+    if o.device != q.device or lse.device != q.device:
+        raise ValueError("o and lse must be on q's device (%s)" % q.device)
+
+
 def _sink_ptr(sink, n_h):
     if sink is None:
         return None
@@ -134,15 +147,17 @@ def fmha_fwd(q, k, v, o=None, lse=None, scale=None, window=0, causal=False, stre
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((b, n_h, T), dtype=torch.float32, device=q.device)
+    qp, kp, vp = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    _check_outputs(q, o, lse)
     if scale is None:
         scale = hd ** -0.5
     if sink is None:
-        rc = load().fmha_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+        rc = load().fmha_fwd(qp, kp, vp, _bf16(o, "o"), _f32(lse, "lse"),
                              b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)),
                              _stream(stream))
         _check(rc, "fmha_fwd")
     else:
-        rc = load().fmha_fwd_sink(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+        rc = load().fmha_fwd_sink(qp, kp, vp, _bf16(o, "o"), _f32(lse, "lse"),
                                   _sink_ptr(sink, n_h), b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
                                   int(bool(causal)), _stream(stream))
         _check(rc, "fmha_fwd_sink")
@@ -290,6 +305,11 @@ def fmha_splitkv_workspace_bytes(batch, n_h, T, hd, n_splits):
     return int(load().fmha_splitkv_workspace_bytes(batch, n_h, T, hd, n_splits))
 
 
+def fmha_workspace_bytes(batch, n_h, T, hd, n_splits):
+    """Bytes of the caller buffers fmha_fwd_splitkv + fmha_merge need for n_splits chunks."""
+    return int(load().fmha_workspace_bytes(batch, n_h, T, hd, n_splits))
+
+
 def fmha_check_device_status(stream=None):
     rc = load().fmha_check_device_status(_stream(stream))
     _check(rc, "fmha_check_device_status")
@@ -332,9 +352,11 @@ def fmha_fwd_noalloc(q, k, v, o, lse, scale=None, window=0, causal=False, stream
     given, and split-KV partials use the library's fixed scratch array instead
     of a workspace (see include/fmha.h)."""
     b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    qp, kp, vp = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    _check_outputs(q, o, lse)
     if scale is None:
         scale = hd ** -0.5
-    rc = load().fmha_fwd_noalloc(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+    rc = load().fmha_fwd_noalloc(qp, kp, vp, _bf16(o, "o"), _f32(lse, "lse"),
                                  b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window), int(bool(causal)),
                                  _stream(stream))
     _check(rc, "fmha_fwd_noalloc")

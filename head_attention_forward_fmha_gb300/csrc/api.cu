@@ -143,15 +143,17 @@ SplitPlan split_layout(int T, int s_k, int window, int chunk) {
 }
 
 int sm_count() {
-    static int cache[128] = {};
+    // Per-device cache; any host thread may fill an entry (the value it stores
+    // is the same whichever thread wins).
+    static std::atomic<int> cache[128];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
-    if (!cache[dev]) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // ---------------------------------------------------------------- planning
@@ -575,6 +577,10 @@ size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_spl
     return partial_bytes((long long)batch * n_h * T, hd, n_splits);
 }
 
+size_t fmha_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits) {
+    return fmha_splitkv_workspace_bytes(batch, n_h, T, hd, n_splits);
+}
+
 int fmha_check_device_status(fmha_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
@@ -686,7 +692,10 @@ extern "C" int fmha_fwd_noalloc(const void* q, const void* k, const void* v, voi
         rc = check_chunks(p, sp.n_splits);
         if (rc) return rc;
         if (sp.n_splits == 1) return run_kernel(q, k, v, p, sp, o, lse, nullptr, nullptr, false, stream);
-        const size_t need = partial_bytes(rows, hd, sp.n_splits);
+        // The partial format is fmha_fwd's: fp16 with range factors on the
+        // hd-512 tensor-core kernel, fp32 elsewhere.
+        const bool f16 = use_f16_partials(p);
+        const size_t need = partial_bytes(rows, hd, sp.n_splits, f16);
         if (need > (size_t)FMHA_NOALLOC_SCRATCH_BYTES)
             return fail(FMHA_ERR_WORKSPACE,
                         "fmha_fwd_noalloc: this shape needs %zu bytes of split-KV scratch (%d chunks x %lld rows); "
@@ -695,11 +704,11 @@ extern "C" int fmha_fwd_noalloc(const void* q, const void* k, const void* v, voi
         void* scratch = nullptr;
         rc = noalloc_scratch(&scratch);
         if (rc) return rc;
-        float* o_part = static_cast<float*>(scratch);
-        float* lse_part = o_part + (size_t)sp.n_splits * rows * hd;
-        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, o_part, lse_part, true, stream);
+        const PartialViews pv = partial_views(scratch, rows, hd, sp.n_splits, f16);
+        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, pv.o_part, pv.lse_part, true, stream, f16, pv.range_part);
         if (rc) return rc;
-        cudaError_t e = launch_merge(o_part, lse_part, nullptr, sp.n_splits, rows, hd, false, o, lse, stream);
+        cudaError_t e =
+            launch_merge(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, o, lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
         return FMHA_OK;
     } catch (...) {

@@ -194,8 +194,14 @@ int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* l
                   float scale, int window, int causal, fmha_stream_t stream);
 
 /* Bytes of fp32 partial output (o_parts + lse_parts) that fmha_fwd_splitkv
- * writes for n_splits chunks. */
+ * writes for n_splits chunks: n_splits * batch * n_h * T * (hd + 1) * 4.
+ * Negative arguments give 0. */
 size_t fmha_splitkv_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits);
+
+/* The same number under the name the split-KV workspace query is usually
+ * given: the caller buffers fmha_fwd_splitkv + fmha_merge need for n_splits
+ * chunks (the count fmha_fwd_plan or fmha_split_layout returns). */
+size_t fmha_workspace_bytes(int batch, int n_h, int T, int hd, int n_splits);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FMHA_ERR_DEVICE_BOUNDS if, in a checked build, a kernel's
@@ -288,19 +294,24 @@ int fmha_set_kernel_path(int path);
  * its device memory up front and accounts for every byte, code that runs on a
  * strict memory budget, or a hot loop that must not risk the synchronisation
  * and latency that cudaMalloc/cudaFree (or a pool growing) can bring.  For
- * them this call computes exactly what fmha_fwd computes, with the same plan
- * and the same kernels, and calls no allocating routine: when the plan splits
- * the KV range, the fp32 partials go to one fixed scratch array of
+ * them this call computes what fmha_fwd computes, with the same plan, the
+ * same kernels and the same partial format (fp32, or fp16 with range factors
+ * on the hd-512 tensor-core kernel; see fmha_fwd), so its results are
+ * fmha_fwd's bit for bit, and it calls no allocating routine: when the plan
+ * splits the KV range, the partials go to one fixed scratch array of
  * FMHA_NOALLOC_SCRATCH_BYTES (32 MiB) that is part of the library's device
  * image, so every GPU that loads the library holds it until the process exits.
  *
- * - A shape whose partials (fmha_splitkv_workspace_bytes for fmha_fwd_plan's
- *   chunk count) exceed the scratch is rejected with FMHA_ERR_WORKSPACE and a
+ * - A shape whose partials (fmha_fwd_plan's chunk count times the rows, in
+ *   that format) exceed the scratch is rejected with FMHA_ERR_WORKSPACE and a
  *   message naming both sizes; nothing is launched.  Shapes that fmha_fwd_plan
  *   does not split need no scratch at all.
  * - The first call on each device looks up the scratch's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *   life of the process; make that first call before any stream capture.  The
+ *   library (this call, and the status word every call uses) must not be used
+ *   on a device after cudaDeviceReset: the addresses it kept belong to the
+ *   context that the reset destroyed.
  * - Every call on a device shares the one scratch array, which keeps the last
  *   call's contents.  Nothing in it needs to start at zero: each call writes
  *   every partial before its merge reads it.  Calls whose work overlaps on the

@@ -29,6 +29,8 @@ int main(void) {
           FMHA_ERR_HEADDIM);
     CHECK(fmha_fwd_host(NULL, NULL, NULL, NULL, NULL, 1, 2, 1, 1, 8, 64, 0.125f, 0, 0, NULL) == FMHA_ERR_NULL);
     CHECK(fmha_splitkv_workspace_bytes(2, 8, 1, 128, 4) == (size_t)4 * 16 * (128 * 4 + 4));
+    CHECK(fmha_workspace_bytes(2, 8, 1, 128, 4) == fmha_splitkv_workspace_bytes(2, 8, 1, 128, 4));
+    CHECK(fmha_workspace_bytes(-1, 8, 1, 128, 4) == 0);
     printf("c abi ok\n");
     return 0;
 }

@@ -49,6 +49,36 @@ def test_host_entry_checks():
                               lse=torch.empty(1, 2, 1))    # o of the wrong shape
 
 
+def test_noalloc_refuses_undersized_outputs():
+    """fmha_fwd_noalloc and fmha_fwd take caller buffers for O and LSE; one
+    smaller than the output is refused before any launch (the kernels would
+    write past its end)."""
+    q, k, v = cpu_qkv(b=2, n_h=4, n_kv_h=2, T=3)
+    good_o, good_lse = torch.empty_like(q), torch.empty(2, 4, 3)
+    binding._check_outputs(q, good_o, good_lse)
+    with pytest.raises(ValueError):
+        binding._check_outputs(q, torch.empty(2, 4, 2, 64, dtype=torch.bfloat16), good_lse)   # o one row short
+    with pytest.raises(ValueError):
+        binding._check_outputs(q, good_o, torch.empty(2, 4, 2))                               # lse one row short
+    with pytest.raises(ValueError):
+        binding._check_outputs(q, good_o.reshape(-1), good_lse)                               # o flattened
+    with pytest.raises(ValueError):
+        binding._check_outputs(q, good_o, torch.empty(2, 4, 3, device="meta"))               # another device
+    # Both entry points run the check before calling into the library; with
+    # host tensors the dtype/device check (TypeError) comes first, so the order
+    # is checked by source: _check_outputs precedes the library call.
+    import inspect
+    for fn, call in ((binding.fmha_fwd_noalloc, "fmha_fwd_noalloc("), (binding.fmha_fwd, "fmha_fwd(")):
+        src = inspect.getsource(fn)
+        assert "_check_outputs(q, o, lse)" in src
+        assert src.index("_check_outputs(q, o, lse)") < src.index("load()." + call)
+
+
+def test_workspace_bytes_alias():
+    assert binding.fmha_workspace_bytes(2, 8, 1, 128, 4) == binding.fmha_splitkv_workspace_bytes(2, 8, 1, 128, 4)
+    assert binding.fmha_workspace_bytes(3, 5, 7, 512, 2) == 2 * 3 * 5 * 7 * (512 + 1) * 4
+
+
 def test_merge_checks():
     with pytest.raises(ValueError):
         binding.fmha_merge(torch.empty(2, 1, 2, 1), torch.empty(2, 1, 2, 1))  # o_parts not 5-D

@@ -11,7 +11,8 @@ run every other test; it also passes on its own in a fresh process.
 import pytest
 import torch
 
-from check_utils import LSE_ATOL, O_ATOL
+from check_utils import LSE_ATOL, O_ATOL, compare, cosine_per_head
+import oracle
 from head_attention_forward_fmha_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -19,25 +20,38 @@ pytestmark = pytest.mark.gpu
 W = inputs.Workload
 
 # Shapes that fmha_fwd splits, so the scratch array is really used: a GQA
-# sliding-window decode with few KV heads (decode kernel) and an MQA decode
-# with many cached keys (tensor-core kernel).
+# sliding-window decode with few KV heads (decode kernel, fp32 partials), an
+# MQA decode with many cached keys (tensor-core kernel, fp32 partials) and the
+# MQA decode at hd 512 (hd-512 tensor-core kernel, fp16 partials with range
+# factors), whose results are also checked against the fp64 oracle.
 SPLIT_SHAPES = [
     W("gqa_swa_decode_b4", 4, 64, 8, 1, 8192, 128, window=4096),
     W("mqa_G128_hd128_long", 2, 128, 1, 1, 4096, 128),
+    W("mqa_decode_hd512", 16, 128, 1, 1, 512, 512),
 ]
+ORACLE_CHECKED = {"mqa_decode_hd512"}
 
 
 def _plan(w):
-    return binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal)
+    return binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal, with_kernel=True)
+
+
+def _scratch_need(w, n_splits, kernel):
+    """Bytes of partials fmha_fwd_noalloc keeps in its scratch: fp16 O plus fp32
+    LSE and two fp32 range factors per row on the hd-512 tensor-core kernel,
+    fp32 O and LSE elsewhere."""
+    rows = w.batch * w.n_h * w.T
+    if w.hd == 512 and kernel == "fwd_tc_wide":
+        return n_splits * rows * (w.hd * 2 + 12)
+    return binding.fmha_splitkv_workspace_bytes(w.batch, w.n_h, w.T, w.hd, n_splits)
 
 
 @pytest.mark.parametrize("w", SPLIT_SHAPES, ids=[w.name for w in SPLIT_SHAPES])
 def test_noalloc_matches_fmha_fwd_on_two_calls(w):
     binding.fmha_set_kernel_path(0)
-    n_splits, _ = _plan(w)
+    n_splits, _, kernel = _plan(w)
     assert n_splits > 1, "shape must exercise the split-KV scratch"
-    need = binding.fmha_splitkv_workspace_bytes(w.batch, w.n_h, w.T, w.hd, n_splits)
-    assert need <= binding.NOALLOC_SCRATCH_BYTES
+    assert _scratch_need(w, n_splits, kernel) <= binding.NOALLOC_SCRATCH_BYTES
     for call, seed in enumerate((21, 22)):       # two calls in a row, different inputs
         q, k, v = inputs.make_inputs(w, seed=seed, device="cuda")
         o_ref, lse_ref = binding.fmha_fwd(q, k, v, scale=w.scale, window=w.window, causal=w.causal)
@@ -49,6 +63,13 @@ def test_noalloc_matches_fmha_fwd_on_two_calls(w):
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), "call %d left outputs unwritten" % call
         assert (o.float() - o_ref.float()).abs().max().item() <= O_ATOL, "call %d: O differs" % call
         assert (lse - lse_ref).abs().max().item() <= LSE_ATOL, "call %d: LSE differs" % call
+        # same plan, kernels and partial format: the same bits
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), "call %d: not fmha_fwd's bits" % call
+        if w.name in ORACLE_CHECKED:
+            bits = [inputs.bf16_bits(t.cpu()) for t in (q, k, v)]
+            o_or, lse_or = oracle.attention(*bits, w.scale, w.window, w.causal)
+            compare(o, lse, o_or, lse_or, "%s call %d vs oracle" % (w.name, call))
+            cosine_per_head(o, o_or, "%s call %d vs oracle" % (w.name, call))
 
 
 def test_noalloc_unsplit_shape_needs_no_scratch():
@@ -63,16 +84,24 @@ def test_noalloc_unsplit_shape_needs_no_scratch():
     assert (lse - lse_ref).abs().max().item() <= LSE_ATOL
 
 
+# MQA prefills at hd 256 with 100 query heads over long caches: 12,800 query
+# rows (25,600 for batch 2) whose fp32 partials take ~13 MB per KV chunk, and
+# the plan splits them into 2-4 chunks (~50 MB).  The first one this GPU's
+# plan splits beyond the scratch is used.
+OVERSIZE = [W("oversize_b1_sk16k", 1, 100, 1, 128, 16384, 256),
+            W("oversize_b2_sk8k", 2, 100, 1, 128, 8192, 256),
+            W("oversize_b1_sk32k", 1, 100, 1, 128, 32768, 256)]
+
+
 def test_noalloc_rejects_partials_larger_than_the_scratch():
-    # MHA prefill at hd 512, 100 heads, 4096 cached keys: the plan splits the
-    # keys in two, and the fp32 partials of 12,800 query rows need ~52 MB, more
-    # than the scratch.  The call is refused before anything runs, so the
-    # inputs need no values.
-    w = W("oversize", 1, 100, 100, 128, 4096, 512)
-    n_splits, _ = _plan(w)
-    need = binding.fmha_splitkv_workspace_bytes(w.batch, w.n_h, w.T, w.hd, n_splits)
-    if need <= binding.NOALLOC_SCRATCH_BYTES:
-        pytest.skip("this GPU's plan for the shape fits the scratch (%d bytes)" % need)
+    # The call is refused before anything runs, so the inputs need no values.
+    for w in OVERSIZE:
+        n_splits, _, kernel = _plan(w)
+        need = _scratch_need(w, n_splits, kernel)
+        if n_splits > 1 and need > binding.NOALLOC_SCRATCH_BYTES:
+            break
+    else:
+        pytest.skip("this GPU's plans for the oversize shapes fit the scratch")
     q = torch.empty((w.batch, w.n_h, w.T, w.hd), dtype=torch.bfloat16, device="cuda")
     k = torch.empty((w.batch, w.n_kv_h, w.s_k, w.hd), dtype=torch.bfloat16, device="cuda")
     v = torch.empty_like(k)
