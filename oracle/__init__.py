@@ -48,6 +48,8 @@ def _bind(path):
     lib.oracle_merge.restype = None
     lib.oracle_split_layout.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32)]
     lib.oracle_split_layout.restype = i32
+    lib.oracle_quantize_nvfp4.argtypes = [vp, i64, i32, ctypes.c_float, vp, vp]
+    lib.oracle_quantize_nvfp4.restype = i32
     lib.oracle_set_threads.argtypes = [i32]
     lib.oracle_max_threads.restype = i32
     return lib
@@ -186,5 +188,37 @@ def merge(o_parts, lse_parts, sink=None):
     return o, lse
 
 
+def quantize_nvfp4(x, global_scale=1.0):
+    """NVFP4 quantisation of rows of fp32 values (the format ``fmha_oracle.c``
+    states): x [..., hd] float32 with hd a multiple of 16.  Returns (codes
+    [..., hd / 2] uint8, two E2M1 codes per byte, element 2i in the low
+    nibble; scales [..., hd / 16] uint8 E4M3 codes)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    hd = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1], dtype=np.int64))
+    codes = np.empty(x.shape[:-1] + (hd // 2,), np.uint8)
+    scales = np.empty(x.shape[:-1] + (hd // 16,), np.uint8)
+    rc = _load().oracle_quantize_nvfp4(x.ctypes.data, rows, hd, float(global_scale), codes.ctypes.data,
+                                       scales.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the NVFP4 arguments (hd %% 16 == 0, global_scale > 0 finite)")
+    return codes, scales
+
+
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def dequantize_nvfp4(codes, scales, global_scale=1.0):
+    """Values g * s * e of NVFP4 codes and E4M3 scales (float64 [..., hd])."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (codes.shape[-1] * 2,))
+    e = _E2M1[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+    c = scales.astype(np.int64)
+    ex, m = c >> 3, c & 7
+    s = np.where(ex == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(ex - 7.0))
+    return float(global_scale) * np.repeat(s, 16, axis=-1) * e
+
+
 __all__ = ["attention", "attention_rows", "split_layout", "partials", "merge",
-           "set_threads", "max_threads"]
+           "quantize_nvfp4", "dequantize_nvfp4", "set_threads", "max_threads"]

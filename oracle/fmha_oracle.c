@@ -51,6 +51,10 @@
  *    so a row with no attended key has O = 0 and lse = sigma_h, and
  *    sigma_h = -inf is no sink at all.  For split-KV the partials carry no
  *    sink and the merge adds it once to its denominator.
+ *  - NVFP4 output (the "register slot for FP4 pack" of [C]'s TMEM-epilogue
+ *    part; the pages' quantiser part names an E2M1 element nibble, an E4M3
+ *    scale and round-to-nearest-even, and gives no block size): see
+ *    oracle_quantize_nvfp4 below for the format taken.
  */
 #include <math.h>
 #include <stdint.h>
@@ -277,4 +281,102 @@ int oracle_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+
+/* ------------------------------------------------------------------------
+ * NVFP4 quantisation of output rows.
+ *
+ * Format (readings; the pages fix only the element and scale types and the
+ * rounding rule):
+ *  - each row of hd values is cut into blocks of 16 consecutive elements;
+ *  - block scale: s = E4M3(amax / (6 g)), amax = max |x_i| over the block,
+ *    g = a global fp32 scale given by the caller (> 0); E4M3 is 1 sign, 4
+ *    exponent bits (bias 7), 3 mantissa bits, subnormals below 2^-6, largest
+ *    finite value 448 (code 0x7F is NaN and never produced);
+ *  - element code: E2M1(x_i / (g s)): magnitude in {0, 0.5, 1, 1.5, 2, 3, 4,
+ *    6} by code 0..7 (1 sign, 2 exponent bits, 1 mantissa bit), sign in bit 3
+ *    (set only for a negative value whose magnitude code is not 0);
+ *  - both roundings: to the nearest representable value, a tie going to the
+ *    even code (mantissa bit 0), and values beyond the largest finite value
+ *    saturate to it;
+ *  - s = 0 (an all-zero block, or amax / (6 g) rounding to 0) gives 0 codes;
+ *  - a value is recovered as g * s * e;
+ *  - storage: codes[row][hd / 2] bytes, element 2i in the low nibble of
+ *    byte i; scales[row][hd / 16] E4M3 bytes.
+ * The pages' final threshold list for the E2M1 rounding (0.25, 0.75, 1.25,
+ * 1.75, 2.75, 3.75, 5.25) agrees with the midpoints of the E2M1 grid up to
+ * 1.75 only (the midpoints of 2|3, 3|4 and 4|6 are 2.5, 3.5 and 5); the
+ * plain definition above is taken instead.
+ * Precision: amax / (6 g) and x_i / (g s) are evaluated in fp32 (the product
+ * 6 g and g s rounded to fp32 first), as the kernels do, so that both sides
+ * take every rounding decision on the same fp32 number.
+ * ------------------------------------------------------------------------ */
+
+/* value of E4M3 code c (0 .. 0x7E), non-negative */
+static double e4m3_value(int c)
+{
+    int e = c >> 3, m = c & 7;
+    if (e == 0) return ldexp((double)m / 8.0, -6);
+    return ldexp(1.0 + (double)m / 8.0, e - 7);
+}
+
+/* nearest E4M3 code to a >= 0, ties to the even code, saturating at 448 */
+static int e4m3_code_rne(double a)
+{
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d_new = fabs(a - e4m3_value(c)), d_best = fabs(a - e4m3_value(best));
+        if (d_new < d_best || (d_new == d_best && (c & 1) == 0)) best = c;
+    }
+    return best;
+}
+
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* nearest E2M1 magnitude code to a >= 0, ties to the even code, saturating at 6 */
+static int e2m1_code_rne(double a)
+{
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        double d_new = fabs(a - kE2M1[c]), d_best = fabs(a - kE2M1[best]);
+        if (d_new < d_best || (d_new == d_best && (c & 1) == 0)) best = c;
+    }
+    return best;
+}
+
+/* x: rows x hd fp32 values (hd a multiple of 16); g: global scale (> 0).
+ * Writes codes [rows][hd / 2] and scales [rows][hd / 16].  Returns 0, or -1
+ * for an invalid argument. */
+int oracle_quantize_nvfp4(const float* x, long rows, int hd, float g, uint8_t* codes, uint8_t* scales)
+{
+    if (rows < 0 || hd <= 0 || hd % 16 != 0 || !(g > 0.0f) || isinf(g)) return -1;
+    for (long r = 0; r < rows; ++r) {
+        for (int blk = 0; blk < hd / 16; ++blk) {
+            const float* xb = x + (size_t)r * hd + blk * 16;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                if (fabsf(xb[i]) > amax) amax = fabsf(xb[i]);
+            const float six_g = 6.0f * g;
+            const float sv = amax / six_g;
+            const int sc = e4m3_code_rne((double)sv);
+            const float s = (float)e4m3_value(sc);
+            scales[(size_t)r * (hd / 16) + blk] = (uint8_t)sc;
+            for (int i = 0; i < 16; i += 2) {
+                int nib[2];
+                for (int h = 0; h < 2; ++h) {
+                    int code = 0;
+                    if (s > 0.0f) {
+                        const float gs = g * s;
+                        const float y = xb[i + h] / gs;
+                        code = e2m1_code_rne(fabs((double)y));
+                        if (y < 0.0f && code != 0) code |= 8;
+                    }
+                    nib[h] = code;
+                }
+                codes[(size_t)r * (hd / 2) + blk * 8 + i / 2] = (uint8_t)(nib[0] | (nib[1] << 4));
+            }
+        }
+    }
+    return 0;
 }

@@ -10,7 +10,11 @@ row), split-KV merge equal to the single pass, and the unmasked case equal to
 states: one more logit in the denominator only) the same brute force with the
 sink's column, Q = 0 giving lse = ln(n + e^sigma), sigma = -inf equal to no
 sink, an empty key range giving lse = sigma, and the split merge adding the
-sink once.  ``test_pins_catch_planted_mistakes`` plants
+sink once; for the NVFP4 output quantisation (the format the oracle states)
+hand-worked blocks (``tests/golden/nvfp4_hand_worked.json``), the E2M1
+rounding against a construction from Python's round-half-even, the E4M3 scale
+against torch's float8_e4m3fn cast, exact round trips of representable blocks
+and the half-step error bound.  ``test_pins_catch_planted_mistakes`` plants
 plausible mistakes in a copy of the oracle's C source and checks that the pins
 reject every one.
 """
@@ -365,12 +369,104 @@ def pin_sink_split_merge_equals_single_pass():
         np.testing.assert_allclose(lm, l1, rtol=0, atol=1e-12)
 
 
+# ----------------------------------------------------------------------------
+# NVFP4 quantisation (the format the oracle states: 16-element blocks, E2M1
+# codes, E4M3 scale of amax / (6 g), both roundings to nearest-even, saturating)
+# ----------------------------------------------------------------------------
+NVFP4_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "nvfp4_hand_worked.json")
+
+
+def pin_nvfp4_golden_blocks():
+    for c in json.load(open(NVFP4_GOLDEN))["cases"]:
+        x = np.asarray(c["x"], dtype=np.float32)[None]
+        codes, scales = oracle.quantize_nvfp4(x, c["global_scale"])
+        assert list(scales[0]) == c["scales"], (c["name"], list(scales[0]))
+        assert list(codes[0]) == c["codes"], (c["name"], list(codes[0]))
+
+
+def _e2m1_by_round(a):
+    """E2M1 magnitude code of a >= 0 built from Python's round() (half to even)
+    on the exponent / mantissa view: step 0.5 below 2, 1 in [2, 4), 2 in [4, 6]."""
+    if a >= 6.0:
+        return 7
+    if a < 2.0:
+        return round(a * 2.0)           # codes 0..4 are 0, 0.5, 1, 1.5, 2
+    if a < 4.0:
+        return round(a) + 2             # 2, 3, 4 -> codes 4, 5, 6
+    return 6 if round(a / 2.0) == 2 else 7
+
+
+def pin_nvfp4_e2m1_rounding_matches_round_half_even():
+    rng = np.random.default_rng(21)
+    ys = np.concatenate([rng.uniform(0, 6, 600), np.arange(0, 6.01, 0.25)]).astype(np.float32)
+    # one block per value: amax 6 (s = 1) so the element is quantised as is
+    # (saturation beyond 6 is covered by the hand-worked blocks)
+    x = np.zeros((ys.size, 16), np.float32)
+    x[:, 0] = 6.0
+    x[:, 1] = ys
+    codes, scales = oracle.quantize_nvfp4(x)
+    assert (scales == 56).all()
+    got = (codes[:, 0] >> 4) & 7
+    want = np.array([_e2m1_by_round(float(y)) for y in ys])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(ys[i]), int(got[i]), int(want[i])) for i in bad[:5]]
+
+
+def pin_nvfp4_e4m3_scale_matches_torch_float8():
+    # amax / 6 for amax = 6 v is exactly v when v has at most 20 significant
+    # bits; torch's float8_e4m3fn cast (round-to-nearest-even) gives its code
+    rng = np.random.default_rng(22)
+    v = np.concatenate([np.exp2(rng.uniform(-11, 8.8, 800)), [2.0 ** -10, 3 * 2.0 ** -11, 1.0625, 1.1875, 240.0]])
+    v = v[v <= 448.0]
+    m, e = np.frexp(v)
+    v = np.ldexp(np.round(m * 2 ** 20) / 2 ** 20, e).astype(np.float32)
+    x = np.zeros((v.size, 16), np.float32)
+    x[:, 3] = 6.0 * v
+    assert (x[:, 3] / np.float32(6.0) == v).all()
+    _, scales = oracle.quantize_nvfp4(x)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = np.nonzero(scales[:, 0] != want)[0]
+    assert bad.size == 0, [(float(v[i]), int(scales[i, 0]), int(want[i])) for i in bad[:5]]
+
+
+def pin_nvfp4_round_trip_of_representable_blocks():
+    # blocks of s * E2M1 values with s an E4M3 value and amax = 6 s come back exactly
+    rng = np.random.default_rng(23)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    for trial in range(50):
+        s = float(np.ldexp(1.0 + rng.integers(0, 8) / 8.0, int(rng.integers(-6, 6))))
+        g = float(rng.choice([0.5, 1.0, 4.0]))
+        e = grid[rng.integers(0, 8, 32)] * rng.choice([-1.0, 1.0], 32)
+        e[0], e[16] = 6.0, -6.0
+        x = (g * s * e).astype(np.float32)[None]
+        codes, scales = oracle.quantize_nvfp4(x, g)
+        np.testing.assert_array_equal(oracle.dequantize_nvfp4(codes, scales, g), x.astype(np.float64))
+
+
+def pin_nvfp4_error_bound_on_random_rows():
+    # |x - deq| <= half the E2M1 step at |x| / (g s), times g s, away from saturation
+    rng = np.random.default_rng(24)
+    x = (rng.standard_normal((64, 64)) * np.exp2(rng.uniform(-4, 4, (64, 1)))).astype(np.float32)
+    codes, scales = oracle.quantize_nvfp4(x, 1.0)
+    deq = oracle.dequantize_nvfp4(codes, scales, 1.0)
+    c = scales.astype(np.int64)
+    s = np.where(c >> 3 == 0, (c & 7) / 8.0 * 2.0 ** -6, (1 + (c & 7) / 8.0) * np.exp2((c >> 3) - 7.0))
+    s = np.repeat(s, 16, axis=-1)
+    y = np.abs(x) / s
+    half_step = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+    inside = y <= 6.0
+    assert (np.abs(x - deq)[inside] <= (half_step * s)[inside] * (1 + 1e-6)).all()
+
+
 ALL_PINS = [pin_golden_cases, pin_brute_force_tiny, pin_softmax_rows_sum_to_one,
             pin_uniform_v_returns_v, pin_key_permutation_invariance, pin_q_zero_closed_form,
             pin_dominant_key, pin_single_attended_key, pin_split_merge_equals_single_pass,
             pin_split_layout, pin_torch_softmax_unmasked, pin_bf16_widening_is_exact,
             pin_rows_api_matches_full, pin_sink_brute_force_tiny, pin_sink_q_zero_closed_form,
-            pin_sink_neg_inf_is_no_sink, pin_sink_empty_key_range, pin_sink_split_merge_equals_single_pass]
+            pin_sink_neg_inf_is_no_sink, pin_sink_empty_key_range, pin_sink_split_merge_equals_single_pass,
+            pin_nvfp4_golden_blocks, pin_nvfp4_e2m1_rounding_matches_round_half_even,
+            pin_nvfp4_e4m3_scale_matches_torch_float8, pin_nvfp4_round_trip_of_representable_blocks,
+            pin_nvfp4_error_bound_on_random_rows]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
@@ -397,6 +493,17 @@ MUTANTS = {
     "sink_per_kv_head": ("sink ? sink[h] : -INFINITY", "sink ? sink[kvh] : -INFINITY"),
     "sink_empty_row_lse": ("*lse_out = sink;  /* -inf without a sink */", "*lse_out = -INFINITY;"),
     "merge_sink_dropped": ("if (sg != -INFINITY) den += exp(sg - mx);", ";"),
+    "nvfp4_e2m1_ties_up": ("if (d_new < d_best || (d_new == d_best && (c & 1) == 0)) best = c;\n    }\n    return best;\n}\n\n/* x:",
+                           "if (d_new <= d_best) best = c;\n    }\n    return best;\n}\n\n/* x:"),
+    "nvfp4_e4m3_ties_up": ("if (d_new < d_best || (d_new == d_best && (c & 1) == 0)) best = c;\n    }\n    return best;\n}\n\nstatic const",
+                           "if (d_new <= d_best) best = c;\n    }\n    return best;\n}\n\nstatic const"),
+    "nvfp4_amax_over_4": ("const float six_g = 6.0f * g;", "const float six_g = 4.0f * g;"),
+    "nvfp4_half_block_amax": ("for (int i = 0; i < 16; ++i)\n                if (fabsf(xb[i]) > amax)",
+                              "for (int i = 0; i < 8; ++i)\n                if (fabsf(xb[i]) > amax)"),
+    "nvfp4_sign_dropped": ("if (y < 0.0f && code != 0) code |= 8;", ";"),
+    "nvfp4_nibble_order": ("(uint8_t)(nib[0] | (nib[1] << 4))", "(uint8_t)(nib[1] | (nib[0] << 4))"),
+    "nvfp4_e4m3_no_saturation": ("for (int c = 1; c <= 0x7E; ++c)", "for (int c = 1; c <= 0x7F; ++c)"),
+    "nvfp4_global_scale_ignored": ("const float gs = g * s;", "const float gs = s;"),
     "merge_sink_in_numerator": ("        if (sg != -INFINITY) den += exp(sg - mx);",
                                 "        if (sg != -INFINITY) { den += exp(sg - mx); orow[0] += exp(sg - mx); }"),
 }
