@@ -52,6 +52,9 @@ SIGNATURES = {
     "fmha_build_flags": ([], _i32),
     "fmha_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "fmha_selftest_bounds_check": ([_vp], _i32),
+    "fmha_fwd_nvfp4": ([_vp, _vp, _vp, _vp, _vp, _vp, _f32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp],
+                       _i32),
+    "fmha_quantize_nvfp4": ([_vp, ctypes.c_longlong, _i32, _f32, _vp, _vp, _vp], _i32),
 }
 # Size of the fixed split-KV scratch fmha_fwd_noalloc uses (FMHA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -317,6 +320,52 @@ def fmha_check_device_status(stream=None):
 
 def fmha_get_last_error():
     return load().fmha_get_last_error().decode(errors="replace")
+
+
+def _u8(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA uint8 tensor" % name)
+    return t.data_ptr()
+
+
+def fmha_fwd_nvfp4(q, k, v, codes=None, scales=None, lse=None, global_scale=1.0, scale=None, window=0,
+                   causal=False, stream=None):
+    """fmha_fwd with O quantised to NVFP4 (see include/fmha.h): returns
+    (codes uint8 [b,n_h,T,hd/2], scales uint8 [b,n_h,T,hd/16] E4M3, lse fp32 [b,n_h,T])."""
+    b, n_h, n_kv_h, T, s_k, hd = _shapes(q, k, v)
+    if codes is None:
+        codes = torch.empty((b, n_h, T, hd // 2), dtype=torch.uint8, device=q.device)
+    if scales is None:
+        scales = torch.empty((b, n_h, T, hd // 16), dtype=torch.uint8, device=q.device)
+    if lse is None:
+        lse = torch.empty((b, n_h, T), dtype=torch.float32, device=q.device)
+    qp, kp, vp = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    if (tuple(codes.shape) != (b, n_h, T, hd // 2) or tuple(scales.shape) != (b, n_h, T, hd // 16)
+            or tuple(lse.shape) != (b, n_h, T)):
+        raise ValueError("codes [b,n_h,T,hd/2], scales [b,n_h,T,hd/16] and lse [b,n_h,T] expected")
+    if codes.device != q.device or scales.device != q.device or lse.device != q.device:
+        raise ValueError("codes, scales and lse must be on q's device (%s)" % q.device)
+    if scale is None:
+        scale = hd ** -0.5
+    rc = load().fmha_fwd_nvfp4(qp, kp, vp, _u8(codes, "codes"), _u8(scales, "scales"), _f32(lse, "lse"),
+                               float(global_scale), b, n_h, n_kv_h, T, s_k, hd, float(scale), int(window),
+                               int(bool(causal)), _stream(stream))
+    _check(rc, "fmha_fwd_nvfp4")
+    return codes, scales, lse
+
+
+def fmha_quantize_nvfp4(x, global_scale=1.0, stream=None):
+    """NVFP4 codes and E4M3 scales of fp32 rows x [..., hd] (the fused epilogues' quantiser)."""
+    if x.dim() < 1 or x.shape[-1] % 16 != 0:
+        raise ValueError("x [..., hd] with hd a multiple of 16 expected")
+    hd = x.shape[-1]
+    rows = x.numel() // hd
+    codes = torch.empty(tuple(x.shape[:-1]) + (hd // 2,), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(tuple(x.shape[:-1]) + (hd // 16,), dtype=torch.uint8, device=x.device)
+    rc = load().fmha_quantize_nvfp4(_f32(x, "x"), rows, hd, float(global_scale), _u8(codes, "codes"),
+                                    _u8(scales, "scales"), _stream(stream))
+    _check(rc, "fmha_quantize_nvfp4")
+    return codes, scales
 
 
 def fmha_release():

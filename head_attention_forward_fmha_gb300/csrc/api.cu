@@ -340,10 +340,15 @@ int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long sla
 // kernel only).
 // sink: [n_h] attention-sink logits for the final output (NULL: none; never
 // applied to partials, whose merge adds it).
+// fp4: when fp4.codes is set, the final output is NVFP4 (o is unused).
 int run_kernel(const void* q, const void* k, const void* v, const Problem& p, const SplitPlan& sp, void* o,
                float* lse, void* o_part, float* lse_part, bool to_partials, cudaStream_t stream,
-               bool f16_parts = false, float* range_part = nullptr, const float* sink = nullptr) {
-    if (to_partials) sink = nullptr;
+               bool f16_parts = false, float* range_part = nullptr, const float* sink = nullptr,
+               Fp4Out fp4 = Fp4Out{nullptr, nullptr, 1.f}) {
+    if (to_partials) {
+        sink = nullptr;
+        fp4.codes = nullptr;
+    }
     unsigned* status = device_status_word();
     if (!status) return fail(FMHA_ERR_LAUNCH, "cannot resolve the device status word");
     const Path path = choose_path(p);
@@ -358,6 +363,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.range_part = range_part;
         L.to_partials = to_partials;
         L.sink = sink;
+        L.fp4 = fp4;
         L.f16_partials = f16_parts;
         if (f16_parts && (path != Path::TensorCoreWide || !range_part || !to_partials))
             return fail(FMHA_ERR_LAUNCH, "fp16 partials need the hd-512 kernel and a range array");
@@ -366,9 +372,11 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.status = status;
         int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, kRowsBf16, "Q");
         if (rc) return rc;
+        // An NVFP4 output is stored row by row without a tensor map; the O map
+        // is then built over Q (same shape and type) and never stored through.
         rc = to_partials ? make_rows_map(&L.tmap_o, o_part, p.hd, p.R, slabs * sp.n_splits,
                                          f16_parts ? kRowsF16 : kRowsF32, "O partials")
-                         : make_rows_map(&L.tmap_o, o, p.hd, p.R, slabs, kRowsBf16, "O");
+                         : make_rows_map(&L.tmap_o, fp4.codes ? q : o, p.hd, p.R, slabs, kRowsBf16, "O");
         if (rc) return rc;
         rc = make_kv_map(&L.tmap_k, k, p.hd, p.s_k, slabs, ks.kv_tile);
         if (rc) return rc;
@@ -387,6 +395,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
     L.lse_part = lse_part;
     L.to_partials = to_partials;
     L.sink = sink;
+    L.fp4 = fp4;
     L.p = p;
     L.sp = sp;
     L.status = status;
@@ -441,6 +450,62 @@ int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* l
 int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int n_h, int n_kv_h,
              int T, int s_k, int hd, float scale, int window, int causal, fmha_stream_t stream) {
     return fmha_fwd_sink(q, k, v, o, lse, nullptr, batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, stream);
+}
+
+int fmha_fwd_nvfp4(const void* q, const void* k, const void* v, void* o_codes, void* o_scales, float* lse,
+                   float o_global_scale, int batch, int n_h, int n_kv_h, int T, int s_k, int hd, float scale,
+                   int window, int causal, fmha_stream_t stream) {
+    try {
+        Problem p;
+        int rc = check_shape(batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, &p);
+        if (rc) return rc;
+        rc = check_inputs(q, k, v, s_k);
+        if (rc) return rc;
+        if (!o_codes || !o_scales || !lse) return fail(FMHA_ERR_NULL, "o_codes, o_scales and lse must be non-NULL");
+        if (!aligned(o_codes, 16) || !aligned(o_scales, 4) || !aligned(lse, 4))
+            return fail(FMHA_ERR_ALIGN, "o_codes must be 16-byte, o_scales and lse 4-byte aligned");
+        if (!(o_global_scale > 0.f) || !std::isfinite(o_global_scale))
+            return fail(FMHA_ERR_SHAPE, "o_global_scale must be finite and > 0");
+        const long long rows = (long long)batch * n_h * T;
+        if (rows == 0) return FMHA_OK;
+        const Fp4Out fp4{static_cast<uint8_t*>(o_codes), static_cast<uint8_t*>(o_scales), o_global_scale};
+        const SplitPlan sp = choose_split(p);
+        rc = check_chunks(p, sp.n_splits);
+        if (rc) return rc;
+        if (sp.n_splits == 1)
+            return run_kernel(q, k, v, p, sp, nullptr, lse, nullptr, nullptr, false, stream, false, nullptr, nullptr,
+                              fp4);
+        void* ws = nullptr;
+        const bool f16 = use_f16_partials(p);
+        rc = workspace(stream, partial_bytes(rows, hd, sp.n_splits, f16), &ws);
+        if (rc) return rc;
+        const PartialViews pv = partial_views(ws, rows, hd, sp.n_splits, f16);
+        rc = run_kernel(q, k, v, p, sp, nullptr, nullptr, pv.o_part, pv.lse_part, true, stream, f16, pv.range_part);
+        if (rc) return rc;
+        cudaError_t e = launch_merge_nvfp4(pv.o_part, pv.lse_part, pv.range_part, sp.n_splits, rows, hd, f16, fp4, lse,
+                                           stream);
+        if (e != cudaSuccess) return cuda_fail(e, "NVFP4 merge kernel launch");
+        return FMHA_OK;
+    } catch (...) {
+        return fail(FMHA_ERR_LAUNCH, "unexpected host exception in fmha_fwd_nvfp4");
+    }
+}
+
+int fmha_quantize_nvfp4(const float* x, long long rows, int hd, float global_scale, void* codes, void* scales,
+                        fmha_stream_t stream) {
+    if (rows < 0 || hd < 16 || hd % 16 != 0)
+        return fail(FMHA_ERR_SHAPE, "fmha_quantize_nvfp4: need rows >= 0 and hd a positive multiple of 16");
+    if (!(global_scale > 0.f) || !std::isfinite(global_scale))
+        return fail(FMHA_ERR_SHAPE, "fmha_quantize_nvfp4: global_scale must be finite and > 0");
+    if (rows == 0) return FMHA_OK;
+    if (!x || !codes || !scales) return fail(FMHA_ERR_NULL, "fmha_quantize_nvfp4: NULL buffer");
+    if (!aligned(x, 16) || !aligned(codes, 8))
+        return fail(FMHA_ERR_ALIGN, "fmha_quantize_nvfp4: x must be 16-byte, codes 8-byte aligned");
+    if (rows > (1LL << 40) / hd) return fail(FMHA_ERR_SHAPE, "fmha_quantize_nvfp4: too many elements");
+    cudaError_t e = launch_quantize_nvfp4(x, rows, hd, global_scale, static_cast<uint8_t*>(codes),
+                                          static_cast<uint8_t*>(scales), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "NVFP4 quantisation kernel launch");
+    return FMHA_OK;
 }
 
 int fmha_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,

@@ -7,6 +7,19 @@
 
 namespace fmha {
 
+// Final-output epilogue of a kernel (a compile-time choice, so that the
+// plain kernels carry none of the other code): bf16 O, bf16 O with an
+// attention sink in the softmax denominator, or NVFP4 O (16-element blocks
+// of E2M1 codes with E4M3 scales, see nvfp4.cuh).
+enum Epilogue : int { kEpiBf16 = 0, kEpiSink = 1, kEpiNvfp4 = 2 };
+
+// NVFP4 output buffers: codes [rows, hd / 2], scales [rows, hd / 16], global scale g.
+struct Fp4Out {
+    uint8_t* codes;
+    uint8_t* scales;
+    float g;
+};
+
 // One attention problem, validated by the API layer.
 struct Problem {
     int batch, n_h, n_kv_h, T, s_k, hd;
@@ -30,6 +43,7 @@ struct DecodeLaunch {
     float* lse_part;
     bool to_partials;
     const float* sink;  // [n_h] attention-sink logits or NULL; applied when !to_partials
+    Fp4Out fp4;         // NVFP4 final output when fp4.codes != NULL (no sink, !to_partials)
     CUtensorMap tmap_k, tmap_v;
     Problem p;
     SplitPlan sp;
@@ -49,6 +63,7 @@ struct TcLaunch {
     bool to_partials;
     const float* sink;  // [n_h] attention-sink logits or NULL; applied when !to_partials
     bool f16_partials;  // hd-512 kernel only
+    Fp4Out fp4;         // NVFP4 final output when fp4.codes != NULL (no sink, !to_partials)
     CUtensorMap tmap_q, tmap_k, tmap_v;
     // bf16 O [slabs, R, hd] (box 64 x 128), fp32 partials [n_splits*slabs, R, hd]
     // (box 32 x 128) or fp16 partials (box 64 x 128)
@@ -84,6 +99,13 @@ inline cudaLaunchAttribute programmatic_launch_attr() {
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
                          long long rows, int hd, bool f16_parts, void* o, float* lse, cudaStream_t stream,
                          const float* sink = nullptr, int T = 1, int n_h = 1);
+// The merge writing NVFP4 O (fp4.codes / fp4.scales) instead of bf16 O; no sink.
+cudaError_t launch_merge_nvfp4(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                               long long rows, int hd, bool f16_parts, Fp4Out fp4, float* lse, cudaStream_t stream);
+
+// ---- NVFP4 quantisation of fp32 rows on its own (nvfp4_kernel.cu) ---------
+cudaError_t launch_quantize_nvfp4(const float* x, long long rows, int hd, float g, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream);
 
 // ---- device status word (status.cu) ---------------------------------------
 // Address of the status word on the current device (nullptr on failure).

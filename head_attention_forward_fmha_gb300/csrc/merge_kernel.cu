@@ -15,6 +15,7 @@
 // Launched as a programmatic dependent: its blocks are scheduled while the
 // split kernel runs and wait in grid_dependency_wait for the partials.
 #include "internal.h"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace fmha {
@@ -251,7 +252,96 @@ cudaError_t launch_hd(const void* o_parts, const float* lse_parts, const float* 
                         sink, T, n_h, status);
 }
 
+// The merge with an NVFP4 final output: one thread per (row, 16-column
+// block).  The weights are the bf16 merge's, exp(lse_i - max) (times the range
+// factor of fp16 partials), one divide by their sum; the 16 merged values are
+// quantised in registers (nvfp4.cuh).  Consecutive threads take consecutive
+// blocks of a row, so each partial's row is read in contiguous 64-byte
+// (fp32) or 32-byte (fp16) pieces.
+template <int HD, typename PT>
+__global__ void __launch_bounds__(256)
+    merge_lse_nvfp4_kernel(const PT* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                           const float* __restrict__ range_parts, int n_splits, long long rows, Fp4Out fp4,
+                           float* __restrict__ lse, unsigned* status) {
+    grid_dependency_wait();  // partials of the preceding split kernel are complete and visible
+    launch_dependents();
+    constexpr int NBLK = HD / 16;
+    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr float kLn2 = 0.693147180559945309f;
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows * NBLK) return;
+    const long long row = t / NBLK;
+    const int blk = (int)(t - row * NBLK);
+    const int col = blk * 16;
+    if (!FMHA_IN_BOUNDS(row >= 0 && row < rows && col + 16 <= HD, kSiteMergeFp4, status)) return;
+    float m = -INFINITY;
+    for (int i = 0; i < n_splits; ++i) m = fmaxf(m, __ldg(lse_parts + (long long)i * rows + row));
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    float den = 0.f;
+    if (m != -INFINITY) {
+        for (int i = 0; i < n_splits; ++i) {
+            const float w = exp2f((__ldg(lse_parts + (long long)i * rows + row) - m) * kLog2e);
+            den += w;
+            float f = w;
+            if constexpr (sizeof(PT) == 2) f *= __ldg(range_parts + ((long long)i * rows + row) * 2 + col / 256);
+            const PT* src = o_parts + ((long long)i * rows + row) * HD + col;
+#pragma unroll
+            for (int q = 0; q < 16; q += 8 / (int)sizeof(PT) * 2) {
+                float v[8 / sizeof(PT) * 2];
+                load_vec<8 / sizeof(PT) * 2>(src + q, v);
+#pragma unroll
+                for (int e = 0; e < (int)(8 / sizeof(PT) * 2); ++e) acc[q + e] += f * v[e];
+            }
+        }
+    }
+    const float inv = (den > 0.f) ? 1.f / den : 0.f;
+    float xb[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xb[e] = acc[e] * inv;
+    uint32_t pk[2];
+    const uint32_t sc = nvfp4_block(xb, fp4.g, pk);
+    *reinterpret_cast<uint2*>(fp4.codes + row * (HD / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+    fp4.scales[row * NBLK + blk] = (uint8_t)sc;
+    if (blk == 0) lse[row] = (den > 0.f) ? m + log2f(den) * kLn2 : -INFINITY;
+}
+
+template <int HD>
+cudaError_t launch_nvfp4_hd(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                            long long rows, bool f16, Fp4Out fp4, float* lse, cudaStream_t stream, unsigned* status) {
+    const long long threads = rows * (HD / 16);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (f16) {
+        if (HD != 512 || range_parts == nullptr) return cudaErrorInvalidValue;
+        return cudaLaunchKernelEx(&cfg, merge_lse_nvfp4_kernel<HD, __half>, static_cast<const __half*>(o_parts),
+                                  lse_parts, range_parts, n_splits, rows, fp4, lse, status);
+    }
+    return cudaLaunchKernelEx(&cfg, merge_lse_nvfp4_kernel<HD, float>, static_cast<const float*>(o_parts), lse_parts,
+                              range_parts, n_splits, rows, fp4, lse, status);
+}
+
 }  // namespace
+
+cudaError_t launch_merge_nvfp4(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
+                               long long rows, int hd, bool f16, Fp4Out fp4, float* lse, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    unsigned* status = device_status_word();
+    if (!status) return cudaErrorInvalidDevicePointer;
+    switch (hd) {
+        case 64: return launch_nvfp4_hd<64>(o_parts, lse_parts, range_parts, n_splits, rows, f16, fp4, lse, stream, status);
+        case 128: return launch_nvfp4_hd<128>(o_parts, lse_parts, range_parts, n_splits, rows, f16, fp4, lse, stream, status);
+        case 256: return launch_nvfp4_hd<256>(o_parts, lse_parts, range_parts, n_splits, rows, f16, fp4, lse, stream, status);
+        case 512: return launch_nvfp4_hd<512>(o_parts, lse_parts, range_parts, n_splits, rows, f16, fp4, lse, stream, status);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_merge(const void* o_parts, const float* lse_parts, const float* range_parts, int n_splits,
                          long long rows, int hd, bool f16, void* o, float* lse, cudaStream_t stream,

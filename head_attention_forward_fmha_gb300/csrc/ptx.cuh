@@ -53,6 +53,7 @@ enum CheckSite : unsigned {
     kSiteTcSCol = 0x106,    // TMEM columns of the S buffer
     kSiteTcPRow = 0x107,    // row of the P buffer
     kSiteTcLse = 0x108,     // LSE / partial LSE index
+    kSiteTcFp4 = 0x109,     // NVFP4 output row
     kSiteWideItem = 0x201,  // ring slot and box coordinates of a producer item
     kSiteWideQ = 0x202,     // resident-Q box coordinates
     kSiteWideVSlots = 0x203,  // the V_ITEMS slots of a PV MMA are consecutive
@@ -61,6 +62,7 @@ enum CheckSite : unsigned {
     kSiteWidePRow = 0x206,
     kSiteWideLse = 0x207,
     kSiteWideRange = 0x208,  // range factor index of an fp16 partial
+    kSiteWideFp4 = 0x209,    // NVFP4 output row
     kSiteDecQRow = 0x301,    // Q row loaded from global memory
     kSiteDecQSmem = 0x302,   // Q staging offset
     kSiteDecKVLoad = 0x303,  // K/V stage: first key, stage offset
@@ -69,11 +71,12 @@ enum CheckSite : unsigned {
     kSiteDecLdsmV = 0x306,   // ldmatrix address inside the V tile
     kSiteDecComb = 0x307,    // combine buffer index
     kSiteDecMl = 0x308,      // per-key-group (max, sum) index
-    kSiteDecOut = 0x309,     // output / partial row
+    kSiteDecOut = 0x309,     // output / partial row (and NVFP4 output block)
     kSiteMergePart = 0x401,  // partial (split, row, column) index
     kSiteMergeRange = 0x402,
     kSiteMergeOut = 0x403,
     kSiteMergeSink = 0x404,
+    kSiteMergeFp4 = 0x405,   // NVFP4 output block of the merge
     kSiteEpiRow = 0x501,     // staging row of the TMA-store epilogue
     kSiteEpiStore = 0x502,   // TMA store box coordinates
     kSiteSink = 0x503,       // sink logit head index

@@ -40,6 +40,7 @@ const char* check_site_name(unsigned site) {
         case kSiteTcSCol: return "row-tile kernel: TMEM columns of S";
         case kSiteTcPRow: return "row-tile kernel: P row";
         case kSiteTcLse: return "row-tile kernel: LSE index";
+        case kSiteTcFp4: return "row-tile kernel: NVFP4 output row";
         case kSiteWideItem: return "hd-512 kernel: producer item slot / coordinates";
         case kSiteWideQ: return "hd-512 kernel: resident Q box coordinates";
         case kSiteWideVSlots: return "hd-512 kernel: V slots of a PV MMA not consecutive";
@@ -48,6 +49,7 @@ const char* check_site_name(unsigned site) {
         case kSiteWidePRow: return "hd-512 kernel: P row";
         case kSiteWideLse: return "hd-512 kernel: LSE index";
         case kSiteWideRange: return "hd-512 kernel: range factor index";
+        case kSiteWideFp4: return "hd-512 kernel: NVFP4 output row";
         case kSiteDecQRow: return "decode kernel: Q row";
         case kSiteDecQSmem: return "decode kernel: Q staging offset";
         case kSiteDecKVLoad: return "decode kernel: K/V stage key / slot";
@@ -61,6 +63,7 @@ const char* check_site_name(unsigned site) {
         case kSiteMergeRange: return "merge: range factor index";
         case kSiteMergeOut: return "merge: output row / column";
         case kSiteMergeSink: return "merge: sink head index";
+        case kSiteMergeFp4: return "merge: NVFP4 output block";
         case kSiteEpiRow: return "epilogue: staging row";
         case kSiteEpiStore: return "epilogue: TMA store coordinates";
         case kSiteSink: return "sink head index";

@@ -2,6 +2,7 @@
 // tc_wide_kernel.cu): the per-row online-softmax step, the write of P into the
 // K-major 128-byte-swizzled operand layout, and the TMA-store epilogue.
 #pragma once
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace fmha {
@@ -183,6 +184,42 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, in
         }
     }
     if (leader) tma_store_wait_read();
+}
+
+// NVFP4 epilogue: this thread's O row (NCOL fp32 columns in TMEM from t_col)
+// times `inv`, quantised in registers (see nvfp4.cuh) 32 columns at a time:
+// two blocks give 16 bytes of codes and two scale bytes, stored straight to
+// global memory.  codes_row / scales_row point at this row's first block in
+// [rows, hd / 2] and [rows, hd / 16]; a row outside the tensor (valid false)
+// stores nothing but still takes part in the warp-collective TMEM loads.
+template <int NCOL>
+__device__ __forceinline__ void epilogue_nvfp4(uint32_t t_col, float inv, bool valid, uint8_t* codes_row,
+                                               uint8_t* scales_row, float g, bool have_o) {
+#pragma unroll 1
+    for (int c = 0; c < NCOL / 32; ++c) {
+        float ov[32];
+        if (have_o) {
+            tmem_ld32(t_col + c * 32, ov);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
+        if (!valid) continue;
+        uint32_t pk[4], sc[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float xb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xb[i] = ov[b * 16 + i] * inv;
+            uint32_t w[2];
+            sc[b] = nvfp4_block(xb, g, w);
+            pk[2 * b] = w[0];
+            pk[2 * b + 1] = w[1];
+        }
+        *reinterpret_cast<uint4*>(codes_row + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint16_t*>(scales_row + c * 2) = (uint16_t)(sc[0] | (sc[1] << 8));
+    }
 }
 
 }  // namespace fmha

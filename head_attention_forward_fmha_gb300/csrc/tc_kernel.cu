@@ -79,6 +79,7 @@ struct TcArgs {
     long long rows_total;
     unsigned* status;
     const float* sink;  // [n_h] sink logits (final output only) or NULL
+    Fp4Out fp4;         // NVFP4 final output (EPI == kEpiNvfp4)
 };
 
 __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, int& hi) {
@@ -89,12 +90,13 @@ __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, i
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <int HD, bool SINK>
+template <int HD, int EPI>
 __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const TcArgs a) {
     using C = TCfg<HD>;
     constexpr int BM = C::BM, BN = C::BN, KST = C::KST, VST = C::VST;
+    constexpr bool SINK = EPI == kEpiSink;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -385,7 +387,16 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
         // the slab's end fall outside the tensor map and are not written.
         uint8_t* stage = sk;
         constexpr int kStageBytes = (KST + VST) * C::KV_TILE;
-        if (!a.to_partials)
+        if constexpr (EPI == kEpiNvfp4) {
+            // quantised in registers and stored per row; rows past the slab's
+            // end and blocks that gave up store nothing
+            named_barrier_sync(2, 128);
+            const long long gr = row0 + grow;
+            const bool row_ok = valid && *abort_flag == 0 &&
+                                FMHA_IN_BOUNDS(gr >= 0 && gr < a.rows_total, kSiteTcFp4, a.status);
+            epilogue_nvfp4<HD>(t_lane + C::O_COL, inv, row_ok, a.fp4.codes + (row_ok ? gr : 0) * (HD / 2),
+                               a.fp4.scales + (row_ok ? gr : 0) * (HD / 16), a.fp4.g, ok && n_tiles > 0);
+        } else if (!a.to_partials)
             epilogue_tma_store<HD, kOutBf16>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo, 0, r_begin,
                                              slab, make_int3(HD, a.R, (int)gridDim.z), ok && n_tiles > 0,
                                              threadIdx.x == 64, abort_flag, a.status);
@@ -412,10 +423,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     }
 }
 
-template <int HD, bool SINK>
+template <int HD, int EPI>
 cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     using C = TCfg<HD>;
-    auto kern = fwd_tc_kernel<HD, SINK>;
+    auto kern = fwd_tc_kernel<HD, EPI>;
     static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -445,6 +456,7 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     a.sink = L.sink;
+    a.fp4 = L.fp4;
     dim3 grid((L.p.R + C::BM - 1) / C::BM, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -470,18 +482,19 @@ int tc_kv_tile(int hd) {
 
 bool tc_supports(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
-template <bool SINK>
+template <int EPI>
 cudaError_t launch_hd(const TcLaunch& L, cudaStream_t stream) {
     switch (L.p.hd) {
-        case 64: return launch_t<64, SINK>(L, stream);
-        case 128: return launch_t<128, SINK>(L, stream);
-        case 256: return launch_t<256, SINK>(L, stream);
+        case 64: return launch_t<64, EPI>(L, stream);
+        case 128: return launch_t<128, EPI>(L, stream);
+        case 256: return launch_t<256, EPI>(L, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream) {
-    return (L.sink && !L.to_partials) ? launch_hd<true>(L, stream) : launch_hd<false>(L, stream);
+    if (L.fp4.codes && !L.to_partials) return launch_hd<kEpiNvfp4>(L, stream);
+    return (L.sink && !L.to_partials) ? launch_hd<kEpiSink>(L, stream) : launch_hd<kEpiBf16>(L, stream);
 }
 
 }  // namespace fmha

@@ -73,6 +73,7 @@ struct WideArgs {
     long long rows_total;
     unsigned* status;
     const float* sink;  // [n_h] sink logits (final output only) or NULL
+    Fp4Out fp4;         // NVFP4 final output (EPI == kEpiNvfp4)
 };
 
 __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, int& hi) {
@@ -83,13 +84,14 @@ __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <bool SINK, bool QRES>
+template <int EPI, bool QRES>
 __global__ void __launch_bounds__(WCfg::THREADS, 1)
     fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                        const WideArgs a) {
     using C = WCfgT<QRES>;
     constexpr int BM = C::BM, BN = C::BN;
+    constexpr bool SINK = EPI == kEpiSink;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -413,7 +415,18 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         const int pslab = split * (int)(a.rows_total / a.R) + slab;
         constexpr int kStageBytes = (QRES ? C::Q_CHUNKS : C::NSLOT) * C::SLOT_BYTES;
         const int3 ext = make_int3(C::HD, a.R, (int)(a.to_partials ? gridDim.y * gridDim.z : gridDim.z));
-        if (!a.to_partials)
+        if constexpr (EPI == kEpiNvfp4) {
+            // quantised in registers and stored per row; rows past the slab's
+            // end and blocks that gave up store nothing
+            named_barrier_sync(2, 128);
+            const long long gr = row0 + grow;
+            const bool row_ok = valid && *abort_flag == 0 &&
+                                FMHA_IN_BOUNDS(gr >= 0 && gr < a.rows_total && (half == 0 || half == 1),
+                                               kSiteWideFp4, a.status);
+            const long long r = row_ok ? gr : 0;
+            epilogue_nvfp4<C::HALF>(t_lane + C::O_COL, inv, row_ok, a.fp4.codes + r * (C::HD / 2) + half * (C::HALF / 2),
+                                    a.fp4.scales + r * (C::HD / 16) + half * (C::HALF / 16), a.fp4.g, have_o);
+        } else if (!a.to_partials)
             epilogue_tma_store<C::HALF, kOutBf16>(t_lane + C::O_COL, inv, row, stage, kStageBytes, &tmo,
                                                   half * C::HALF, r_begin, slab, ext, have_o, threadIdx.x == 64,
                                                   abort_flag, a.status);
@@ -450,7 +463,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
 int tc_wide_kv_tile() { return WCfg::BN; }
 
-template <bool SINK, bool QRES>
+template <int EPI, bool QRES>
 cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     using C = WCfgT<QRES>;
     static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
@@ -458,7 +471,7 @@ cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<SINK, QRES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<EPI, QRES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 128) attr_set[dev] = true;
@@ -484,6 +497,7 @@ cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     a.sink = L.sink;
+    a.fp4 = L.fp4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * ((L.p.R + C::BM - 1) / C::BM), L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cfg.blockDim = dim3(C::THREADS);
@@ -492,18 +506,19 @@ cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<SINK, QRES>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<EPI, QRES>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
 }
 
-template <bool SINK>
+template <int EPI>
 cudaError_t launch_wide_q(const TcLaunch& L, cudaStream_t stream) {
     // Q stays resident when a block may see two or more 128-key tiles.
     const int span = std::min(L.sp.kv_chunk, L.p.s_k);
-    return span > WCfg::BN ? launch_wide_t<SINK, true>(L, stream) : launch_wide_t<SINK, false>(L, stream);
+    return span > WCfg::BN ? launch_wide_t<EPI, true>(L, stream) : launch_wide_t<EPI, false>(L, stream);
 }
 
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {
-    return (L.sink && !L.to_partials) ? launch_wide_q<true>(L, stream) : launch_wide_q<false>(L, stream);
+    if (L.fp4.codes && !L.to_partials) return launch_wide_q<kEpiNvfp4>(L, stream);
+    return (L.sink && !L.to_partials) ? launch_wide_q<kEpiSink>(L, stream) : launch_wide_q<kEpiBf16>(L, stream);
 }
 
 }  // namespace fmha

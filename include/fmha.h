@@ -193,6 +193,42 @@ int fmha_fwd_sink(const void* q, const void* k, const void* v, void* o, float* l
                   int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
                   float scale, int window, int causal, fmha_stream_t stream);
 
+/*
+ * fmha_fwd with the output O quantised to NVFP4 in the epilogue, from the fp32
+ * values that would otherwise be rounded to bf16 (commit 593bc25 of the
+ * pages, TMEM-epilogue part: "register slot for FP4 pack"; its quantiser part
+ * names an E2M1 element nibble, an E4M3 scale and round-to-nearest-even, and
+ * gives no block size).  Format taken:
+ *   - each O row [hd] is cut into hd / 16 blocks of 16 consecutive elements;
+ *   - block scale s = E4M3(amax / (6 g)), amax the block's largest |O|, g =
+ *     o_global_scale (finite, > 0); E4M3: 4 exponent bits (bias 7), 3
+ *     mantissa bits, subnormals, largest finite value 448;
+ *   - element code e = E2M1(O / (g s)): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ *     for codes 0..7, sign in bit 3 (never set on a zero magnitude);
+ *   - both roundings go to the nearest representable value, a tie to the even
+ *     code, and saturate at the largest finite value; s = 0 gives codes 0;
+ *   - amax / (6 g) and O / (g s) are IEEE fp32 divisions;
+ *   - O is recovered as g * s * e.
+ * o_codes:  [batch, n_h, T, hd / 2] bytes, element 2i in the low nibble of
+ *           byte i of its row; 16-byte aligned.
+ * o_scales: [batch, n_h, T, hd / 16] E4M3 bytes; 4-byte aligned.
+ * lse as fmha_fwd.  No attention sink.  Plan, kernels, workspace, errors and
+ * asynchrony are fmha_fwd's; when the plan splits, the merge quantises.
+ */
+int fmha_fwd_nvfp4(const void* q, const void* k, const void* v, void* o_codes, void* o_scales, float* lse,
+                   float o_global_scale, int batch, int n_h, int n_kv_h, int T, int s_k, int hd,
+                   float scale, int window, int causal, fmha_stream_t stream);
+
+/*
+ * The NVFP4 quantisation of fmha_fwd_nvfp4 applied to fp32 rows on their own:
+ * x [rows, hd] fp32 (hd a multiple of 16, x 16-byte aligned) -> codes
+ * [rows, hd / 2] (8-byte aligned) and scales [rows, hd / 16], with the same
+ * block quantiser the fused epilogues run, so its codes can be checked bit
+ * for bit.  Stream-ordered; FMHA_ERR_SHAPE for a bad hd, rows or global scale.
+ */
+int fmha_quantize_nvfp4(const float* x, long long rows, int hd, float global_scale, void* codes, void* scales,
+                        fmha_stream_t stream);
+
 /* Bytes of fp32 partial output (o_parts + lse_parts) that fmha_fwd_splitkv
  * writes for n_splits chunks: n_splits * batch * n_h * T * (hd + 1) * 4.
  * Negative arguments give 0. */

@@ -141,6 +141,29 @@ def test_fwd_sink_argument_errors(lib):
 
 
 
+def test_nvfp4_argument_errors(lib):
+    # every call here fails its argument checks (or has nothing to do) before
+    # any launch: the fake pointers are never dereferenced
+    f = lib.fmha_fwd_nvfp4
+    # q, k, v, codes, scales, lse, g, batch, n_h, n_kv_h, T, s_k, hd, scale, window, causal, stream
+    assert f(16, 16, 16, 0, 16, 16, 1.0, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -1     # codes NULL
+    assert f(16, 16, 16, 16, 0, 16, 1.0, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -1     # scales NULL
+    assert f(16, 16, 16, 24, 16, 16, 1.0, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -2    # codes misaligned
+    assert f(16, 16, 16, 16, 18, 16, 1.0, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -2    # scales misaligned
+    for g in (0.0, -1.0, float("inf"), float("nan")):
+        assert f(16, 16, 16, 16, 16, 16, g, 1, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == -5
+    assert f(16, 16, 16, 16, 16, 16, 1.0, 1, 2, 1, 1, 8, 96, 0.125, 0, 0, None) == -3
+    assert f(16, 16, 16, 16, 16, 16, 1.0, 0, 2, 1, 1, 8, 64, 0.125, 0, 0, None) == 0     # empty problem
+    qz = lib.fmha_quantize_nvfp4
+    assert qz(16, 4, 24, 1.0, 16, 16, None) == -5                                       # hd not a multiple of 16
+    assert qz(16, -1, 32, 1.0, 16, 16, None) == -5
+    assert qz(16, 4, 32, 0.0, 16, 16, None) == -5
+    assert qz(16, 0, 32, 1.0, 0, 0, None) == 0                                          # nothing to do
+    assert qz(0, 4, 32, 1.0, 16, 16, None) == -1
+    assert qz(8, 4, 32, 1.0, 16, 16, None) == -2                                        # x misaligned
+    assert qz(16, 4, 32, 1.0, 12, 16, None) == -2                                       # codes misaligned
+
+
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(ImportError):
         binding.load(str(tmp_path / "nope.so"))
