@@ -392,7 +392,8 @@ def fmha_selftest_wait_timeout(timeout_us, stream=None):
 
 
 def fmha_set_kernel_path(path):
-    """0 automatic, 1 decode kernel, 2 tensor-core kernel (where hd <= 256)."""
+    """0 automatic, 1 decode kernel, 2 tensor-core kernels, 3 tensor-core kernels with the
+    row-tile kernel's P V in the SS form (P through shared memory) instead of the TS form."""
     _check(load().fmha_set_kernel_path(int(path)), "fmha_set_kernel_path")
 
 

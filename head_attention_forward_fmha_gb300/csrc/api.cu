@@ -163,7 +163,8 @@ int sm_count() {
 // 64 rows at hd <= 128, 32 rows at hd 256 and 512, where the decode kernel's
 // CUDA-core-side work per key grows with hd (measured on the MHA shape sweep).
 int tc_min_rows(int hd) { return hd >= 256 ? 32 : 64; }
-std::atomic<int> g_path_override{0};  // 0 auto, 1 decode kernel, 2 tensor-core kernel
+// 0 auto, 1 decode kernel, 2 tensor-core kernel, 3 tensor-core kernel with the SS-form PV
+std::atomic<int> g_path_override{0};
 
 enum class Path { Decode, TensorCore, TensorCoreWide };
 
@@ -171,7 +172,7 @@ Path choose_path(const Problem& p) {
     const int ov = g_path_override.load();
     const bool tc_ok = tc_supports(p.hd) || p.hd == 512;
     if (ov == 1 || !tc_ok) return Path::Decode;
-    if (ov == 2 || p.R >= tc_min_rows(p.hd)) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
+    if (ov >= 2 || p.R >= tc_min_rows(p.hd)) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
     return Path::Decode;
 }
 
@@ -364,6 +365,7 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.to_partials = to_partials;
         L.sink = sink;
         L.fp4 = fp4;
+        L.ss_pv = g_path_override.load() == 3;
         L.f16_partials = f16_parts;
         if (f16_parts && (path != Path::TensorCoreWide || !range_part || !to_partials))
             return fail(FMHA_ERR_LAUNCH, "fp16 partials need the hd-512 kernel and a range array");
@@ -700,7 +702,8 @@ int fmha_selftest_bounds_check(fmha_stream_t stream) {
 }
 
 int fmha_set_kernel_path(int path) {
-    if (path < 0 || path > 2) return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0, 1 or 2 expected (got %d)", path);
+    if (path < 0 || path > 3)
+        return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0, 1, 2 or 3 expected (got %d)", path);
     g_path_override.store(path);
     return FMHA_OK;
 }

@@ -64,6 +64,7 @@ struct TcLaunch {
     const float* sink;  // [n_h] attention-sink logits or NULL; applied when !to_partials
     bool f16_partials;  // hd-512 kernel only
     Fp4Out fp4;         // NVFP4 final output when fp4.codes != NULL (no sink, !to_partials)
+    bool ss_pv;         // row-tile kernel: P through shared memory (SS-form PV) instead of TMEM (TS form)
     CUtensorMap tmap_q, tmap_k, tmap_v;
     // bf16 O [slabs, R, hd] (box 64 x 128), fp32 partials [n_splits*slabs, R, hd]
     // (box 32 x 128) or fp16 partials (box 64 x 128)

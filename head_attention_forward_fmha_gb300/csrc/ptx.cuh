@@ -54,6 +54,7 @@ enum CheckSite : unsigned {
     kSiteTcPRow = 0x107,    // row of the P buffer
     kSiteTcLse = 0x108,     // LSE / partial LSE index
     kSiteTcFp4 = 0x109,     // NVFP4 output row
+    kSiteTcPTmem = 0x10a,   // TMEM columns of P (TS-form PV)
     kSiteWideItem = 0x201,  // ring slot and box coordinates of a producer item
     kSiteWideQ = 0x202,     // resident-Q box coordinates
     kSiteWideVSlots = 0x203,  // the V_ITEMS slots of a PV MMA are consecutive
@@ -405,6 +406,20 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16: the "TS" form.  A is
+// M x 16 bf16 held in tensor memory, row m in lane m, the 16 reduction-dim
+// elements of the row packed two per 32-bit column over 8 consecutive
+// columns starting at a_tmem (lane field 0).  A and B are both bf16.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on an mbarrier when every tcgen05.mma this thread issued so
 // far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -444,6 +459,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane from raw words
+// (packed bf16 pairs of P for the TS-form MMA).
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 

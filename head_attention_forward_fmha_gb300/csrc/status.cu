@@ -41,6 +41,7 @@ const char* check_site_name(unsigned site) {
         case kSiteTcPRow: return "row-tile kernel: P row";
         case kSiteTcLse: return "row-tile kernel: LSE index";
         case kSiteTcFp4: return "row-tile kernel: NVFP4 output row";
+        case kSiteTcPTmem: return "row-tile kernel: TMEM columns of P (TS-form PV)";
         case kSiteWideItem: return "hd-512 kernel: producer item slot / coordinates";
         case kSiteWideQ: return "hd-512 kernel: resident Q box coordinates";
         case kSiteWideVSlots: return "hd-512 kernel: V slots of a PV MMA not consecutive";

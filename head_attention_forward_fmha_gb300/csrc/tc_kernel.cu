@@ -39,20 +39,25 @@
 namespace fmha {
 namespace {
 
-template <int HD>
+// TS = false: P goes through two shared-memory buffers and PV reads A from
+// shared memory (the "SS" form).  TS = true: the softmax writes P into tensor
+// memory over its own S tile (bf16 pairs in the first BN / 2 columns of the S
+// buffer) and PV reads A from there (the "TS" form); the P buffers' shared
+// memory holds more K / V stages instead.
+template <int HD, bool TS>
 struct TCfg {
     static constexpr int BM = 128;                     // query rows per CTA (MMA M)
     static constexpr int BN = (HD <= 128) ? 128 : 64;  // keys per tile
-    static constexpr int KST = (HD == 64) ? 4 : 2;     // K stages
-    static constexpr int VST = (HD == 64) ? 4 : 2;     // V stages
+    static constexpr int KST = TS ? (HD == 64 ? 6 : 3) : (HD == 64 ? 4 : 2);  // K stages
+    static constexpr int VST = TS ? (HD == 64 ? 6 : HD == 128 ? 3 : 2) : (HD == 64 ? 4 : 2);  // V stages
     static constexpr int NB = HD / 64;                 // 64-column (128-byte) boxes
     static constexpr int Q_BYTES = BM * HD * 2;
     static constexpr int KV_TILE = BN * HD * 2;        // one K or V tile
     static constexpr int P_GROUPS = (BN + 63) / 64;    // 128-byte swizzled row groups of P
     static constexpr int P_CHUNKS = (BN < 64 ? BN : 64) / 8;  // 16-byte chunks per row and group
-    static constexpr int P_BYTES = BM * 128 * P_GROUPS;  // one P buffer (two are kept)
+    static constexpr int P_BYTES = TS ? 0 : BM * 128 * P_GROUPS;  // one P buffer (two are kept)
     static constexpr int THREADS = 224;
-    static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
+    static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers (P over S in TS), then O
     static constexpr int O_COL = 2 * BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;
@@ -90,11 +95,11 @@ __device__ __forceinline__ void attended_rows(int t, const TcArgs& a, int& lo, i
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <int HD, int EPI>
-__global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
+template <int HD, int EPI, bool TS>
+__global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const TcArgs a) {
-    using C = TCfg<HD>;
+    using C = TCfg<HD, TS>;
     constexpr int BM = C::BM, BN = C::BN, KST = C::KST, VST = C::VST;
     constexpr bool SINK = EPI == kEpiSink;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
@@ -289,10 +294,17 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(p_addr + pb * C::P_BYTES + (kk >> 2) * BM * 128 + (kk & 3) * 32,
-                                                        16, 1024);
                     const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, BN * 128, 1024);
-                    tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    if constexpr (TS) {
+                        // A = P_j in TMEM: S buffer j & 1, 8 columns (16 bf16 keys) per MMA
+                        const uint32_t a_col = C::S_COL0 + (j & 1) * BN + kk * 8;
+                        if (!FMHA_IN_BOUNDS(a_col + 8 <= C::S_COL0 + 2 * BN, kSiteTcPTmem, a.status)) break;
+                        tc_mma_f16_ts(tmem + C::O_COL, tmem + a_col, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint64_t ad = smem_desc_sw128(
+                            p_addr + pb * C::P_BYTES + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                        tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 tc_commit(&o_done[pb]);
                 tc_commit(&v_empty[s]);
@@ -342,20 +354,28 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
             uint32_t pk[BN / 2];
             softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-            // P buffer pb was last read by PV_{j-2}; a rescale of O needs PV_{j-1} done.
+            // SS: P buffer pb was last read by PV_{j-2}.  TS: P_j goes over S_j,
+            // whose QK the MMA issuer queued after PV_{j-2}, so S_j being ready
+            // means that PV is done.  Either way a rescale of O needs PV_{j-1} done.
             if (rescale) {
                 if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status)) {
                     ok = false;
                     break;
                 }
-            } else if (j >= 2) {
+            } else if (!TS && j >= 2) {
                 if (!mbar_wait(&o_done[pb], ((j >> 1) - 1) & 1, a.status)) {
                     ok = false;
                     break;
                 }
             }
-            if (FMHA_IN_BOUNDS(row >= 0 && row < BM && pb < 2, kSiteTcPRow, a.status))
+            if constexpr (TS) {
+                // this row's P_j (BN bf16 = BN / 2 words) over the S_j columns it has read
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) tmem_st32u(t_lane + s_col + c * 32, pk + c * 32);
+                tmem_wait_st();
+            } else if (FMHA_IN_BOUNDS(row >= 0 && row < BM && pb < 2, kSiteTcPRow, a.status)) {
                 write_p_row<BN>(sp + pb * C::P_BYTES, row, pk);
+            }
             if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
@@ -369,7 +389,7 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
                 }
                 tmem_wait_st();
             }
-            fence_proxy_async_smem();
+            if constexpr (!TS) fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&p_ready[pb]);
         }
@@ -423,10 +443,10 @@ __global__ void __launch_bounds__(TCfg<HD>::THREADS, 1)
     }
 }
 
-template <int HD, int EPI>
+template <int HD, int EPI, bool TS>
 cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
-    using C = TCfg<HD>;
-    auto kern = fwd_tc_kernel<HD, EPI>;
+    using C = TCfg<HD, TS>;
+    auto kern = fwd_tc_kernel<HD, EPI, TS>;
     static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -473,28 +493,33 @@ cudaError_t launch_t(const TcLaunch& L, cudaStream_t stream) {
 
 int tc_kv_tile(int hd) {
     switch (hd) {
-        case 64: return TCfg<64>::BN;
-        case 128: return TCfg<128>::BN;
-        case 256: return TCfg<256>::BN;
+        case 64: return TCfg<64, true>::BN;
+        case 128: return TCfg<128, true>::BN;
+        case 256: return TCfg<256, true>::BN;
         default: return 0;
     }
 }
 
 bool tc_supports(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
-template <int EPI>
+template <int EPI, bool TS>
 cudaError_t launch_hd(const TcLaunch& L, cudaStream_t stream) {
     switch (L.p.hd) {
-        case 64: return launch_t<64, EPI>(L, stream);
-        case 128: return launch_t<128, EPI>(L, stream);
-        case 256: return launch_t<256, EPI>(L, stream);
+        case 64: return launch_t<64, EPI, TS>(L, stream);
+        case 128: return launch_t<128, EPI, TS>(L, stream);
+        case 256: return launch_t<256, EPI, TS>(L, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+template <int EPI>
+cudaError_t launch_form(const TcLaunch& L, cudaStream_t stream) {
+    return L.ss_pv ? launch_hd<EPI, false>(L, stream) : launch_hd<EPI, true>(L, stream);
+}
+
 cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream) {
-    if (L.fp4.codes && !L.to_partials) return launch_hd<kEpiNvfp4>(L, stream);
-    return (L.sink && !L.to_partials) ? launch_hd<kEpiSink>(L, stream) : launch_hd<kEpiBf16>(L, stream);
+    if (L.fp4.codes && !L.to_partials) return launch_form<kEpiNvfp4>(L, stream);
+    return (L.sink && !L.to_partials) ? launch_form<kEpiSink>(L, stream) : launch_form<kEpiBf16>(L, stream);
 }
 
 }  // namespace fmha

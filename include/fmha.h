@@ -316,8 +316,12 @@ int fmha_selftest_bounds_check(fmha_stream_t stream);
  * Kernel-family selection for every later call in the process: 0 = automatic
  * (default: the 128-row tensor-core kernels when a KV head has at least 64
  * query rows at hd <= 128, or 32 at hd 256 and 512, else the decode kernel),
- * 1 = always the decode kernel, 2 = always the tensor-core kernels.  Meant for tests and
- * measurements that compare the two families on one shape; results agree
+ * 1 = always the decode kernel, 2 = always the tensor-core kernels, 3 = always
+ * the tensor-core kernels, and the row-tile kernel (hd <= 256) with its P V
+ * product in the "SS" form (P staged in shared memory) instead of the default
+ * "TS" form (P written over S in tensor memory and read from there as the
+ * MMA's A operand; CURRENT_ISSUE.md "Next steps", TS MMA for PV).  Meant for
+ * tests and measurements that compare kernels on one shape; results agree
  * within the documented tolerance.  Returns FMHA_ERR_SHAPE for other values.
  */
 int fmha_set_kernel_path(int path);

@@ -1,6 +1,9 @@
 """GPU parity of each kernel family on shapes the automatic choice would send
 to the other one: the decode kernel (mma.sync, 8/16 query rows per block) and
 the 128-row tensor-core kernel (tcgen05 + TMEM), both against the fp64 oracle.
+The row-tile kernel's P V product runs in the TS form by default (P written
+over S in tensor memory, read from there as the MMA's A operand); path 3
+forces the SS form (P through shared memory), and both are checked.
 """
 import numpy as np
 import pytest
@@ -43,11 +46,38 @@ def path():
     binding.fmha_set_kernel_path(0)
 
 
-@pytest.mark.parametrize("which", [1, 2], ids=["decode_kernel", "tensor_core_kernel"])
+@pytest.mark.parametrize("which", [1, 2, 3], ids=["decode_kernel", "tensor_core_kernel_ts", "tensor_core_kernel_ss"])
 @pytest.mark.parametrize("w", SHAPES, ids=[w.name for w in SHAPES])
 def test_kernel_family_matches_oracle(w, which, path):
     path(which)
     (q, k, v), (qd, kd, vd) = device_inputs(w, seed=4)
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    o_ref, lse_ref = oracle_full(w, q, k, v)
+    compare(o, lse, o_ref, lse_ref, "%s/path%d" % (w.name, which))
+    cosine_per_head(o, o_ref, "%s/path%d" % (w.name, which))
+
+
+TS_SHAPES = [
+    # the TS-form PV at every row-tile head dim, with causal, window and both
+    W("ts_hd64_causal", 2, 4, 2, 128, 700, 64, causal=True),
+    W("ts_hd64_window", 1, 8, 4, 64, 900, 64, window=333),
+    W("ts_hd128_causal", 1, 4, 4, 128, 1000, 128, causal=True),
+    W("ts_hd128_window_causal", 2, 8, 2, 32, 777, 128, window=129, causal=True),
+    W("ts_hd256_causal", 1, 4, 4, 128, 512, 256, causal=True),
+    W("ts_hd256_window", 1, 64, 1, 1, 1500, 256, window=1000),
+    W("ts_hd256_window_causal", 1, 2, 2, 100, 640, 256, window=64, causal=True),
+]
+
+
+@pytest.mark.parametrize("which", [2, 3], ids=["ts", "ss"])
+@pytest.mark.parametrize("w", TS_SHAPES, ids=[w.name for w in TS_SHAPES])
+def test_pv_forms_match_oracle(w, which, path):
+    """Row-tile kernel forced, in the TS form (path 2) and the SS form (path 3),
+    against the oracle."""
+    path(which)
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=12)
     o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window, causal=w.causal)
     torch.cuda.synchronize()
     binding.fmha_check_device_status()
