@@ -63,7 +63,6 @@ struct DecodeArgs {
     long long rows_total;  // batch * n_h * T
     unsigned* status;
     const float* sink;     // [n_h] sink logits (final output only) or NULL
-    Fp4Out fp4;            // NVFP4 final output (EPI == kEpiNvfp4)
 };
 
 __device__ __forceinline__ void attended(int t, const DecodeArgs& a, int& lo, int& hi) {
@@ -74,10 +73,14 @@ __device__ __forceinline__ void attended(int t, const DecodeArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
+// fp4: the NVFP4 output buffers, read by the kEpiNvfp4 instantiation only.  They
+// are a parameter of their own: as a DecodeArgs field they changed ptxas's
+// register allocation of the bf16 instantiations (hd 128 with 16 rows went from
+// 147 to 128 registers and ran 11 % slower at s_k 32768).
 template <int HD, int NB, int EPI>
 __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                          const DecodeArgs a) {
+                          const DecodeArgs a, const Fp4Out fp4) {
     using C = DCfg<HD, NB>;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
     extern __shared__ uint8_t smem_raw[];
@@ -343,12 +346,50 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
         }
     named_barrier_sync(1, C::NCW * 32);
 
-    // Sum the key groups, divide once by the running sum (plus the sink), write
-    // out: bf16 O or fp32 partials 8 columns per item, or NVFP4 O one
-    // 16-column block per item (quantised in registers, nvfp4.cuh).
-    constexpr int IW = (EPI == kEpiNvfp4) ? 16 : 8;  // columns per item
-    for (int item = threadIdx.x; item < C::RT * (HD / IW); item += C::NCW * 32) {
-        const int r = item / (HD / IW), di = item - r * (HD / IW);
+    // Sum the key groups, divide once by the running sum (plus the sink), write out.
+    if constexpr (EPI == kEpiNvfp4) {
+        // NVFP4 O: one 16-column block per item, quantised in registers (nvfp4.cuh)
+        for (int item = threadIdx.x; item < C::RT * (HD / 16); item += C::NCW * 32) {
+            const int r = item / (HD / 16), b16 = item - r * (HD / 16);
+            if (r_begin + r >= r_end) continue;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::KW; ++w) M = fmaxf(M, ml[w * C::RT + r].x);
+            const float Mu = (M == -INFINITY) ? 0.f : M;
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::KW; ++w) L += ml[w * C::RT + r].y * exp2f(ml[w * C::RT + r].x - Mu);
+            const long long grow = row0 + r_begin + r;
+            float inv, lse;
+            finish_row(M, L, -INFINITY, inv, lse);
+            float xb[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) xb[e] = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::KW; ++w) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 u = reinterpret_cast<const float4*>(comb + (w * C::RT + r) * HD + b16 * 16)[q4];
+                    xb[4 * q4] += u.x;
+                    xb[4 * q4 + 1] += u.y;
+                    xb[4 * q4 + 2] += u.z;
+                    xb[4 * q4 + 3] += u.w;
+                }
+            }
+            if (!FMHA_IN_BOUNDS(grow >= 0 && grow < a.rows_total && split < (int)gridDim.y, kSiteDecOut, a.status))
+                continue;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) xb[e] *= inv;
+            uint32_t pk[2];
+            const uint32_t sc = nvfp4_block(xb, fp4.g, pk);
+            *reinterpret_cast<uint2*>(fp4.codes + grow * (HD / 2) + b16 * 8) = make_uint2(pk[0], pk[1]);
+            fp4.scales[grow * (HD / 16) + b16] = (uint8_t)sc;
+            if (b16 == 0) a.lse[grow] = lse;
+        }
+        return;
+    }
+    for (int item = threadIdx.x; item < C::RT * (HD / 8); item += C::NCW * 32) {
+        const int r = item / (HD / 8), d8 = item - r * (HD / 8);
         if (r_begin + r >= r_end) continue;
         float M = -INFINITY;
 #pragma unroll
@@ -364,45 +405,32 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
                    (EPI == kEpiSink) ? sink_log2_of(a.sink, kvh * a.group + (r_begin + r) / a.T, a.n_h, a.status)
                                      : -INFINITY,
                    inv, lse);
-        float acc[IW];
+        float acc[8];
 #pragma unroll
-        for (int e = 0; e < IW; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
         for (int w = 0; w < C::KW; ++w) {
-#pragma unroll
-            for (int q4 = 0; q4 < IW / 4; ++q4) {
-                const float4 u = reinterpret_cast<const float4*>(comb + (w * C::RT + r) * HD + di * IW)[q4];
-                acc[4 * q4] += u.x;
-                acc[4 * q4 + 1] += u.y;
-                acc[4 * q4 + 2] += u.z;
-                acc[4 * q4 + 3] += u.w;
-            }
+            const float4* src = reinterpret_cast<const float4*>(comb + (w * C::RT + r) * HD + d8 * 8);
+            const float4 u0 = src[0], u1 = src[1];
+            acc[0] += u0.x; acc[1] += u0.y; acc[2] += u0.z; acc[3] += u0.w;
+            acc[4] += u1.x; acc[5] += u1.y; acc[6] += u1.z; acc[7] += u1.w;
         }
         if (!FMHA_IN_BOUNDS(grow >= 0 && grow < a.rows_total && split < (int)gridDim.y, kSiteDecOut, a.status))
             continue;
-        if constexpr (EPI == kEpiNvfp4) {
-            float xb[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) xb[e] = acc[e] * inv;
-            uint32_t pk[2];
-            const uint32_t sc = nvfp4_block(xb, a.fp4.g, pk);
-            *reinterpret_cast<uint2*>(a.fp4.codes + grow * (HD / 2) + di * 8) = make_uint2(pk[0], pk[1]);
-            a.fp4.scales[grow * (HD / 16) + di] = (uint8_t)sc;
-            if (di == 0) a.lse[grow] = lse;
-        } else if (!a.to_partials) {
+        if (!a.to_partials) {
             uint4 pk;
             pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
             pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
             pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
             pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-            *reinterpret_cast<uint4*>(a.o + grow * HD + di * 8) = pk;
-            if (di == 0) a.lse[grow] = lse;
+            *reinterpret_cast<uint4*>(a.o + grow * HD + d8 * 8) = pk;
+            if (d8 == 0) a.lse[grow] = lse;
         } else {
             const long long prow = (long long)split * a.rows_total + grow;
-            float4* dst = reinterpret_cast<float4*>(a.o_part + prow * HD + di * 8);
+            float4* dst = reinterpret_cast<float4*>(a.o_part + prow * HD + d8 * 8);
             dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
             dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-            if (di == 0) a.lse_part[prow] = lse;
+            if (d8 == 0) a.lse_part[prow] = lse;
         }
     }
 }
@@ -441,7 +469,6 @@ cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     a.rows_total = (long long)L.p.batch * L.p.n_h * L.p.T;
     a.status = L.status;
     a.sink = L.sink;
-    a.fp4 = L.fp4;
     const int row_tiles = (L.p.R + C::RT - 1) / C::RT;
     dim3 grid(row_tiles, L.sp.n_splits, L.p.batch * L.p.n_kv_h);
     cudaLaunchConfig_t cfg = {};
@@ -452,7 +479,7 @@ cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, a);
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, a, L.fp4);
 }
 
 }  // namespace
