@@ -25,8 +25,9 @@ namespace {
 // QRES = false: Q and K chunks stream through one 8-slot ring (a block with
 // a single KV tile reads Q once either way).  QRES = true (blocks with two or
 // more KV tiles): the 128 KB Q tile is loaded once and stays resident, and
-// only K and V chunks stream through a 4-slot ring; the epilogue then stages
-// O in the Q region.
+// only K and V chunks stream through a 6-slot ring; the epilogue then stages
+// O in the Q region.  In both, P goes over S in tensor memory and the P V
+// MMAs read it from there (the TS form), so no shared memory holds P.
 template <bool QRES>
 struct WCfgT {
     static constexpr int HD = 512;
@@ -35,15 +36,19 @@ struct WCfgT {
     static constexpr int BN = 128;
     static constexpr int SLOT_BYTES = 128 * 128;       // 128 rows x 64 bf16 columns
     static constexpr int Q_CHUNKS = HD / 64;
-    static constexpr int NSLOT = QRES ? 4 : 8;
+    static constexpr int NSLOT = QRES ? 6 : 8;
     static constexpr int QK_ITEMS = QRES ? Q_CHUNKS : 2 * Q_CHUNKS;  // (Q chunk +) K chunk per column block
     static constexpr int V_ITEMS = HALF / 64;
     static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
-    // The V items of a tile start at a multiple of V_ITEMS and never wrap the
-    // ring, so they sit in V_ITEMS consecutive slots: PV is one N = 256 MMA
-    // per 16 keys over those slots.
-    static_assert(QK_ITEMS % V_ITEMS == 0 && NSLOT % V_ITEMS == 0, "V slots must be contiguous");
-    static constexpr int P_BYTES = BM * BN * 2;
+    // The V items of a tile start at an index that is a multiple of V_GROUP,
+    // so each group of V_GROUP items sits in consecutive slots: P V is one MMA
+    // of N = 64 V_GROUP per group and 16 keys (one N = 256 MMA with the 8-slot
+    // ring; two N = 128 MMAs with the 6-slot ring, whose tiles' V chunks may
+    // wrap around the ring between the pairs).
+    static constexpr int V_GROUP = (NSLOT % V_ITEMS == 0) ? V_ITEMS : 2;
+    static_assert(QK_ITEMS % V_GROUP == 0 && NSLOT % V_GROUP == 0 && V_ITEMS % V_GROUP == 0,
+                  "V slot groups must be contiguous");
+    static constexpr int P_BYTES = 0;  // P lives in tensor memory
     static constexpr int THREADS = 192;
     static constexpr int O_COL = 2 * BN;
     static constexpr int TMEM_COLS = 512;
@@ -52,7 +57,7 @@ struct WCfgT {
     static constexpr int OFF_P = OFF_RING + NSLOT * SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
     static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging (128 KB)
-    static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + 1 + (QRES ? 1 : 0);
+    static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + 2 + 1 + (QRES ? 1 : 0);
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -96,14 +101,13 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem + C::OFF_RING;
-    uint8_t* sp = smem + C::OFF_P;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* slot_full = bars;
     uint64_t* slot_empty = bars + C::NSLOT;
     uint64_t* s_full = slot_empty + C::NSLOT;  // [2]
-    uint64_t* p_ready = s_full + 2;
-    uint64_t* o_done = p_ready + 1;
-    uint64_t* mma_drain = o_done + 1;  // every MMA the issuer launched has completed (exit drain)
+    uint64_t* p_ready = s_full + 2;    // [2] by S buffer: P_j is in TMEM over S_j
+    uint64_t* o_done = p_ready + 2;    // [2] by S buffer: PV_j completed
+    uint64_t* mma_drain = o_done + 2;  // every MMA the issuer launched has completed (exit drain)
     uint64_t* q_full = mma_drain + 1;  // QRES only
     uint8_t* qres = smem + C::OFF_Q;
     uint8_t* stage = smem + C::OFF_STAGE;
@@ -194,8 +198,10 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         }
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
-        mbar_init(p_ready, 128);
-        mbar_init(o_done, 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(&p_ready[b2], 128);
+            mbar_init(&o_done[b2], 1);
+        }
         mbar_init(mma_drain, 1);
         if (QRES) mbar_init(q_full, 1);
         *abort_flag = 0;
@@ -248,8 +254,8 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, C::HALF, 1);
-            const uint32_t ring_addr = smem_u32(ring), p_addr = smem_u32(sp), q_addr = smem_u32(qres);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, 64 * C::V_GROUP, 1);
+            const uint32_t ring_addr = smem_u32(ring), q_addr = smem_u32(qres);
             int item = 0;
             bool ok = true;
             if (QRES) ok = mbar_wait(q_full, 0, a.status);
@@ -285,28 +291,33 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             ok = issue_qk(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
-                if (!(ok = mbar_wait(p_ready, j & 1, a.status))) break;
+                if (!(ok = mbar_wait(&p_ready[j & 1], (j >> 1) & 1, a.status))) break;
                 tc_fence_after();
-                int sv0 = 0;
+                int sv[C::V_ITEMS];
                 for (int c = 0; c < C::V_ITEMS && ok; ++c) {
-                    int sv;
-                    ok = slot_take(sv);
-                    if (c == 0) sv0 = sv;
-                    if (ok) ok = FMHA_IN_BOUNDS(sv == sv0 + c && sv < C::NSLOT, kSiteWideVSlots, a.status);
+                    ok = slot_take(sv[c]);
+                    if (ok)
+                        ok = FMHA_IN_BOUNDS(sv[c] < C::NSLOT && (c % C::V_GROUP == 0 || sv[c] == sv[c - 1] + 1),
+                                            kSiteWideVSlots, a.status);
                 }
                 if (!ok) break;
                 tc_fence_after();
-                // B: the V_ITEMS 64-column boxes of this half, one slot apart
-                // (the descriptor's leading byte offset); 16 keys per MMA.
+                // A: P_j in TMEM over S_j (8 columns = 16 keys per MMA); B: each
+                // group of V_GROUP 64-column V boxes, one slot apart (the
+                // descriptor's leading byte offset), into its columns of O.
+                const uint32_t p_col = (j & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(p_addr + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd =
-                        smem_desc_sw128(ring_addr + sv0 * C::SLOT_BYTES + kk * 16 * 128, C::SLOT_BYTES, 1024);
-                    tc_mma_f16(tmem + C::O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int g = 0; g < C::V_ITEMS / C::V_GROUP; ++g) {
+                        const uint64_t bd = smem_desc_sw128(
+                            ring_addr + sv[g * C::V_GROUP] * C::SLOT_BYTES + kk * 16 * 128, C::SLOT_BYTES, 1024);
+                        tc_mma_f16_ts(tmem + C::O_COL + g * 64 * C::V_GROUP, tmem + p_col + kk * 8, bd, idesc_o,
+                                      (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                for (int c = 0; c < C::V_ITEMS; ++c) tc_commit(&slot_empty[sv0 + c]);
-                tc_commit(o_done);
+                for (int c = 0; c < C::V_ITEMS; ++c) tc_commit(&slot_empty[sv[c]]);
+                tc_commit(&o_done[j & 1]);
             }
             // Exit drain: whatever the loop issued has completed before TMEM
             // and the operand buffers are released, even if a wait gave up.
@@ -348,13 +359,17 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             float alpha;
             uint32_t pk[BN / 2];
             softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
-            // PV_{j-1} must be complete before P is overwritten and O rescaled.
-            if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
+            // P_j goes over S_j, whose QK the MMA issuer queued after PV_{j-2}, so
+            // S_j being ready means that PV is done; a rescale of O needs PV_{j-1}.
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+            if (rescale && !mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status)) {
                 ok = false;
                 break;
             }
-            if (FMHA_IN_BOUNDS(row >= 0 && row < BM, kSiteWidePRow, a.status)) write_p_row<BN>(sp, row, pk);
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) tmem_st32u(t_lane + s_col + c * 32, pk + c * 32);
+            tmem_wait_st();
+            if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < C::HALF / 32; ++c) {
@@ -367,11 +382,10 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 }
                 tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_ready);
+            mbar_arrive(&p_ready[j & 1]);
         }
-        if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+        if (ok && n_tiles > 0) ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
