@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -144,13 +145,14 @@ SplitPlan split_layout(int T, int s_k, int window, int chunk) {
 
 int sm_count() {
     // Per-device cache; any host thread may fill an entry (the value it stores
-    // is the same whichever thread wins).
+    // is the same whichever thread wins).  Without a device (planning on a
+    // host) the count is GB300's 152 SMs.
     static std::atomic<int> cache[128];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 152;
     int n = cache[dev].load(std::memory_order_relaxed);
     if (!n) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
         cache[dev].store(n, std::memory_order_relaxed);
     }
     return n;
@@ -188,10 +190,15 @@ KernelShape kernel_shape(const Problem& p, Path path) {
 
 // Estimated time (us) of a tensor-core split into n chunks: waves of blocks
 // (one block per SM), each moving its K/V chunk, its Q tile and its output at
-// about 60 GB/s after ~1.5 us of fixed latency, never faster than all bytes at
-// the copy bandwidth, plus for n > 1 the merge (~2.5 us and its partials).
-// The constants are this GPU's measured per-block rates (GB300: a 128-row
-// block streams ~60-75 GB/s; block set-up, softmax tail and epilogue ~1.5 us).
+// its per-block rate after ~1.5 us of fixed latency, never faster than the
+// bytes DRAM serves at the copy bandwidth, plus for n > 1 the merge (~2.5 us
+// and its partials).  Per-block rates measured on GB300: a row-tile block
+// streams ~60 GB/s unless its softmax (~1.05 us per 128 keys for 128 rows)
+// is slower, as at hd 64 (256 bytes of K and V per key: ~31 GB/s); an hd-512
+// block ~52 GB/s (96 KB of K/V in flight, ~1.9 us per ring-slot round trip).
+// The two halves of an hd-512 row tile read the same K, the second from L2,
+// so DRAM serves K and V once per pair of blocks.  At hd 512, s_k 32768
+// (128 row-tile halves) seven chunks measured 891 us against 962 us for one.
 double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long long units, long long sms,
                      long long span, long long n) {
     const long long ctas = units * n;
@@ -203,9 +210,11 @@ double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long lo
     const double q = (double)ks.rows_per_cta * p.hd * 2.0;
     const double part_b = n > 1 ? (wide ? 2.0 : 4.0) : 2.0;
     const double out = (double)ks.rows_per_cta * (p.hd / ks.blocks_per_row_tile) * part_b;
-    const double block_us = 1.5 + (kv + q + out) / 60e3;
+    const double rate = wide ? 52e3 : std::min(60e3, 4.0 * p.hd / (1.05 / 128.0));  // bytes per us
+    const double block_us = 1.5 + (kv + q + out) / rate;
     double t = (double)waves * block_us;
-    const double floor_us = (double)ctas * (kv + q + out) / 6.7e6;
+    const double dram = wide ? (double)keys * 2.0 * p.hd + q / 2.0 + out : kv + q + out;
+    const double floor_us = (double)ctas * dram / 6.7e6;
     if (t < floor_us) t = floor_us;
     if (n > 1) t += 2.5 + (double)p.batch * p.n_h * p.T * p.hd * part_b * (double)n / 10e6;
     return t;
