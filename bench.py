@@ -114,6 +114,7 @@ KERNEL_SOURCES = {
     "decode_splitkv": ("decode_kernel.cu", "ptx.cuh"),
     "fwd_tc": ("tc_kernel.cu", "tc_common.cuh", "ptx.cuh"),
     "fwd_tc_wide": ("tc_wide_kernel.cu", "tc_common.cuh", "ptx.cuh"),
+    "fwd_tc_pair": ("tc_pair_kernel.cu", "tc_common.cuh", "ptx.cuh"),
     "merge_lse": ("merge_kernel.cu", "ptx.cuh"),
 }
 

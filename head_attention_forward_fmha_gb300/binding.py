@@ -195,7 +195,7 @@ def fmha_fwd_host(q, k, v, o=None, lse=None, scale=None, window=0, causal=False,
     return o, lse
 
 
-KERNELS = {1: "decode_splitkv", 2: "fwd_tc", 3: "fwd_tc_wide"}
+KERNELS = {1: "decode_splitkv", 2: "fwd_tc", 3: "fwd_tc_wide", 4: "fwd_tc_pair"}
 
 
 def fmha_fwd_plan(batch, n_h, n_kv_h, T, s_k, hd, window=0, causal=False, with_kernel=False):
@@ -392,8 +392,10 @@ def fmha_selftest_wait_timeout(timeout_us, stream=None):
 
 
 def fmha_set_kernel_path(path):
-    """0 automatic, 1 decode kernel, 2 tensor-core kernels, 3 tensor-core kernels with the
-    row-tile kernel's P V in the SS form (P through shared memory) instead of the TS form."""
+    """0 automatic, 1 decode kernel, 2 tensor-core kernels (two row tiles per block where that
+    kernel applies), 3 tensor-core kernels, one row tile per block, with the row-tile kernel's
+    P V in the SS form (P through shared memory) instead of the TS form, 4 tensor-core kernels,
+    one row tile per block (TS form)."""
     _check(load().fmha_set_kernel_path(int(path)), "fmha_set_kernel_path")
 
 

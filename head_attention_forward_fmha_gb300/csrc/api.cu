@@ -160,23 +160,20 @@ int sm_count() {
 
 // ---------------------------------------------------------------- planning
 // Kernel families: the decode kernel (8 or 16 query rows per thread block,
-// mma.sync) and the tensor-core kernels (128 query rows, tcgen05).  A KV head
-// with at least tc_min_rows(hd) query rows goes to the tensor-core kernels:
-// 64 rows at hd <= 128, 32 rows at hd 256 and 512, where the decode kernel's
-// CUDA-core-side work per key grows with hd (measured on the MHA shape sweep).
+// mma.sync) and the tensor-core kernels (128-row query tiles, tcgen05).  A KV
+// head with at least tc_min_rows(hd) query rows goes to the tensor-core
+// kernels: 64 rows at hd <= 128, 32 rows at hd 256 and 512, where the decode
+// kernel's CUDA-core-side work per key grows with hd (measured on the MHA shape
+// sweep).  At hd 128 a KV head with more than 128 rows may also take the
+// two-row-tile kernel (two tiles per block sharing each K/V tile); the planner
+// picks whichever of the two has the lower estimated time.
 int tc_min_rows(int hd) { return hd >= 256 ? 32 : 64; }
-// 0 auto, 1 decode kernel, 2 tensor-core kernel, 3 tensor-core kernel with the SS-form PV
+// 0 auto, 1 decode kernel, 2 tensor-core kernels (two row tiles per block
+// where the shape allows), 3 tensor-core kernels with the row-tile kernel's
+// SS-form PV, 4 tensor-core kernels with one row tile per block
 std::atomic<int> g_path_override{0};
 
-enum class Path { Decode, TensorCore, TensorCoreWide };
-
-Path choose_path(const Problem& p) {
-    const int ov = g_path_override.load();
-    const bool tc_ok = tc_supports(p.hd) || p.hd == 512;
-    if (ov == 1 || !tc_ok) return Path::Decode;
-    if (ov >= 2 || p.R >= tc_min_rows(p.hd)) return p.hd == 512 ? Path::TensorCoreWide : Path::TensorCore;
-    return Path::Decode;
-}
+enum class Path { Decode, TensorCore, TensorCorePair, TensorCoreWide };
 
 struct KernelShape {
     int rows_per_cta, kv_tile, ctas_per_sm, blocks_per_row_tile, min_chunk;
@@ -184,23 +181,32 @@ struct KernelShape {
 
 KernelShape kernel_shape(const Problem& p, Path path) {
     if (path == Path::TensorCore) return {kTcRows, tc_kv_tile(p.hd), 1, 1, 256};
+    if (path == Path::TensorCorePair) return {2 * kTcRows, tc_pair_kv_tile(), 1, 1, 256};
     if (path == Path::TensorCoreWide) return {kTcRows, tc_wide_kv_tile(), 1, 2, 128};
     return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2, 1, 256};
 }
 
 // Estimated time (us) of a tensor-core split into n chunks: waves of blocks
-// (one block per SM), each moving its K/V chunk, its Q tile and its output at
-// its per-block rate after ~1.5 us of fixed latency, never faster than the
+// (one block per SM), each moving its K/V chunk, its Q tile(s) and its output
+// at its per-block rate after ~1.5 us of fixed latency, never faster than the
 // bytes DRAM serves at the copy bandwidth, plus for n > 1 the merge (~2.5 us
 // and its partials).  Per-block rates measured on GB300: a row-tile block
 // streams ~60 GB/s unless its softmax (~1.05 us per 128 keys for 128 rows)
 // is slower, as at hd 64 (256 bytes of K and V per key: ~31 GB/s); an hd-512
-// block ~52 GB/s (96 KB of K/V in flight, ~1.9 us per ring-slot round trip).
+// block ~52 GB/s (96 KB of K/V in flight, ~1.9 us per ring-slot round trip);
+// at hd <= 128 a row-tile block also needs tile_us_per_128_keys of MMAs and
+// softmax per 128 keys, and a two-row-tile block pair_us_per_128_keys for its
+// two tiles (GQA prefill hd 128, T 128: 80.8 us with one row tile per block
+// and 63.0 us with two, s_k 4096).
 // The two halves of an hd-512 row tile read the same K, the second from L2,
 // so DRAM serves K and V once per pair of blocks.  At hd 512, s_k 32768
 // (128 row-tile halves) seven chunks measured 891 us against 962 us for one.
-double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long long units, long long sms,
+double pair_us_per_128_keys(int) { return 1.9; }
+double tile_us_per_128_keys(int hd) { return hd == 64 ? 1.1 : 1.25; }
+
+double tc_split_cost(const Problem& p, const KernelShape& ks, Path path, long long units, long long sms,
                      long long span, long long n) {
+    const bool wide = path == Path::TensorCoreWide;
     const long long ctas = units * n;
     const long long waves = (ctas + sms - 1) / sms;
     long long keys = (span + n - 1) / n;
@@ -210,8 +216,13 @@ double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long lo
     const double q = (double)ks.rows_per_cta * p.hd * 2.0;
     const double part_b = n > 1 ? (wide ? 2.0 : 4.0) : 2.0;
     const double out = (double)ks.rows_per_cta * (p.hd / ks.blocks_per_row_tile) * part_b;
-    const double rate = wide ? 52e3 : std::min(60e3, 4.0 * p.hd / (1.05 / 128.0));  // bytes per us
-    const double block_us = 1.5 + (kv + q + out) / rate;
+    const double rate = (wide || path == Path::TensorCorePair) ? (wide ? 52e3 : 60e3)
+                                                               : std::min(60e3, 4.0 * p.hd / (1.05 / 128.0));
+    double stream_us = (kv + q + out) / rate;
+    if (path == Path::TensorCorePair) stream_us = std::max(stream_us, (double)keys / 128.0 * pair_us_per_128_keys(p.hd));
+    if (path == Path::TensorCore && p.hd <= 128)
+        stream_us = std::max(stream_us, (double)keys / 128.0 * tile_us_per_128_keys(p.hd));
+    const double block_us = 1.5 + stream_us;
     double t = (double)waves * block_us;
     const double dram = wide ? (double)keys * 2.0 * p.hd + q / 2.0 + out : kv + q + out;
     const double floor_us = (double)ctas * dram / 6.7e6;
@@ -220,12 +231,55 @@ double tc_split_cost(const Problem& p, const KernelShape& ks, bool wide, long lo
     return t;
 }
 
+// Best chunk count of a tensor-core kernel and its estimated time: the count
+// with the least tc_split_cost; a larger count must win by 3 %.
+struct TcChoice {
+    long long n;
+    double us;
+};
+
+TcChoice tc_best_split(const Problem& p, Path path, long long span) {
+    const KernelShape ks = kernel_shape(p, path);
+    const long long units = (long long)p.batch * p.n_kv_h * ((p.R + ks.rows_per_cta - 1) / ks.rows_per_cta) *
+                            ks.blocks_per_row_tile;
+    const long long sms = sm_count();
+    TcChoice best{1, tc_split_cost(p, ks, path, units, sms, span, 1)};
+    if (units <= 0 || span <= ks.min_chunk) return best;
+    long long max_n = span / ks.min_chunk;
+    if (max_n > 64) max_n = 64;
+    for (long long c = 2; c <= max_n; ++c) {
+        const double t = tc_split_cost(p, ks, path, units, sms, span, c);
+        if (t < best.us * 0.97) best = TcChoice{c, t};  // a clear gain only: fewer chunks on near-ties
+    }
+    return best;
+}
+
+long long kv_span(const Problem& p) {
+    const SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
+    return (long long)p.s_k - whole.kv_begin;
+}
+
+Path choose_path(const Problem& p) {
+    const int ov = g_path_override.load();
+    const bool tc_ok = tc_supports(p.hd) || p.hd == 512;
+    if (ov == 1 || !tc_ok) return Path::Decode;
+    if (ov < 2 && p.R < tc_min_rows(p.hd)) return Path::Decode;
+    if (p.hd == 512) return Path::TensorCoreWide;
+    const bool pair_ok = tc_pair_supports(p.hd) && p.R > kTcRows;
+    if (!pair_ok || ov == 3 || ov == 4) return Path::TensorCore;
+    if (ov == 2) return Path::TensorCorePair;
+    const long long span = kv_span(p);
+    return tc_best_split(p, Path::TensorCorePair, span).us < tc_best_split(p, Path::TensorCore, span).us
+               ? Path::TensorCorePair
+               : Path::TensorCore;
+}
+
 // Split heuristic.  Decode kernel: as many chunks as keep every thread block
 // resident in one wave (SMs x blocks per SM); a chunk scan on GB300 (MHA b4
 // h16, hd 64-512, s_k 4096-32768, and the GQA window decode) found the step
 // fastest there, longer chunks amortising each block's fixed latency.  Tensor-core
 // kernels (one block per SM): the chunk count with the least estimated time
-// (tc_split_cost), which weighs wave quantisation against the Q tile each
+// (tc_best_split), which weighs wave quantisation against the Q tile each
 // extra block reloads and the partials it writes.
 SplitPlan choose_split(const Problem& p) {
     const Path path = choose_path(p);
@@ -234,23 +288,12 @@ SplitPlan choose_split(const Problem& p) {
                             ks.blocks_per_row_tile;
     SplitPlan whole = split_layout(p.T, p.s_k, p.window, p.s_k > 0 ? p.s_k : 1);
     const long long span = (long long)p.s_k - whole.kv_begin;
-    const long long sms = sm_count();
     if (units <= 0 || span <= ks.min_chunk) return whole;
     long long n = 1;
     if (path != Path::Decode) {
-        const bool wide = path == Path::TensorCoreWide;
-        long long max_n = span / ks.min_chunk;
-        if (max_n > 64) max_n = 64;
-        double best = tc_split_cost(p, ks, wide, units, sms, span, 1);
-        for (long long c = 2; c <= max_n; ++c) {
-            const double t = tc_split_cost(p, ks, wide, units, sms, span, c);
-            if (t < best * 0.97) {  // a clear gain only: fewer chunks on near-ties
-                best = t;
-                n = c;
-            }
-        }
+        n = tc_best_split(p, path, span).n;
     } else {
-        const long long target = sms * ks.ctas_per_sm;
+        const long long target = (long long)sm_count() * ks.ctas_per_sm;
         if (units >= target) return whole;
         n = target / units;
         const long long max_n = span / ks.min_chunk;
@@ -393,7 +436,13 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         if (rc) return rc;
         rc = make_kv_map(&L.tmap_v, v, p.hd, p.s_k, slabs, ks.kv_tile);
         if (rc) return rc;
-        cudaError_t e = (path == Path::TensorCoreWide) ? launch_tc_wide(L, stream) : launch_tc(L, stream);
+        // The two-row-tile kernel has no NVFP4 epilogue (its O is transposed in
+        // tensor memory): an NVFP4 output takes the one-row-tile kernel, with
+        // the same KV tiles and chunks.
+        const bool pair = path == Path::TensorCorePair && !(fp4.codes && !to_partials);
+        cudaError_t e = (path == Path::TensorCoreWide) ? launch_tc_wide(L, stream)
+                        : pair                         ? launch_tc_pair(L, stream)
+                                                       : launch_tc(L, stream);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
         return FMHA_OK;
     }
@@ -565,7 +614,7 @@ int fmha_fwd_plan(int batch, int n_h, int n_kv_h, int T, int s_k, int hd, int wi
     if (kv_chunk) *kv_chunk = sp.kv_chunk;
     if (kernel) {
         const Path path = choose_path(p);
-        *kernel = path == Path::Decode ? 1 : (path == Path::TensorCore ? 2 : 3);
+        *kernel = path == Path::Decode ? 1 : path == Path::TensorCore ? 2 : path == Path::TensorCoreWide ? 3 : 4;
     }
     return sp.n_splits;
 }
@@ -711,8 +760,8 @@ int fmha_selftest_bounds_check(fmha_stream_t stream) {
 }
 
 int fmha_set_kernel_path(int path) {
-    if (path < 0 || path > 3)
-        return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0, 1, 2 or 3 expected (got %d)", path);
+    if (path < 0 || path > 4)
+        return fail(FMHA_ERR_SHAPE, "fmha_set_kernel_path: 0 to 4 expected (got %d)", path);
     g_path_override.store(path);
     return FMHA_OK;
 }

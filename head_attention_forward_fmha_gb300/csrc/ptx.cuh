@@ -43,7 +43,8 @@ constexpr bool kCheckedBuild = false;
 #endif
 
 // Site codes: 0x1nn row-tile kernel, 0x2nn hd-512 kernel, 0x3nn decode
-// kernel, 0x4nn merge, 0x5nn shared epilogue / softmax helpers.
+// kernel, 0x4nn merge, 0x5nn shared epilogue / softmax helpers, 0x7nn
+// two-row-tile kernel.
 enum CheckSite : unsigned {
     kSiteTcQLoad = 0x101,   // Q box coordinates
     kSiteTcKLoad = 0x102,   // K tile: first key, stage offset
@@ -82,6 +83,13 @@ enum CheckSite : unsigned {
     kSiteEpiStore = 0x502,   // TMA store box coordinates
     kSiteSink = 0x503,       // sink logit head index
     kSiteSelfTest = 0x601,   // fmha_selftest_bounds_check (no access behind it)
+    kSitePairQLoad = 0x701,  // Q box coordinates of either row tile
+    kSitePairKLoad = 0x702,  // K tile: first key, stage offset
+    kSitePairVLoad = 0x703,  // V tile: first key, stage offset
+    kSitePairKDesc = 0x704,  // K stage the QK MMAs read
+    kSitePairVDesc = 0x705,  // V stage the PV MMAs read
+    kSitePairLse = 0x706,    // LSE / partial LSE index
+    kSitePairFp4 = 0x707,    // NVFP4 output row
 };
 
 static __device__ __noinline__ bool bounds_failed(unsigned site, unsigned* status) {

@@ -69,6 +69,13 @@ const char* check_site_name(unsigned site) {
         case kSiteEpiStore: return "epilogue: TMA store coordinates";
         case kSiteSink: return "sink head index";
         case kSiteSelfTest: return "index-check self-test";
+        case kSitePairQLoad: return "two-row-tile kernel: Q box coordinates";
+        case kSitePairKLoad: return "two-row-tile kernel: K tile key / stage";
+        case kSitePairVLoad: return "two-row-tile kernel: V tile key / stage";
+        case kSitePairKDesc: return "two-row-tile kernel: K stage of the QK MMAs";
+        case kSitePairVDesc: return "two-row-tile kernel: V stage of the PV MMAs";
+        case kSitePairLse: return "two-row-tile kernel: LSE index";
+        case kSitePairFp4: return "two-row-tile kernel: NVFP4 output row";
         default: return "unknown site";
     }
 }

@@ -112,7 +112,8 @@ enum OutMode : int {
 //   bf16 / fp16: boxes of 64 columns x 128 rows (128-byte rows, swizzled);
 //   fp32: boxes of 32 columns x 128 rows.
 // Box b of the stage sits at stage + b * 16 KB.  All 128 threads of the four
-// softmax warps call this together; thread `leader` issues the stores (the
+// softmax warps call this together (they meet at named barrier `bar_id`,
+// which no other thread uses meanwhile); thread `leader` issues the stores (the
 // TMA store of commit e4ee9fd: bulk_group, commit_group, wait_group.read 0).
 // Boxes are stored as soon as they are staged, so the TMA reads box b while
 // the threads stage box b + 1; only the last read is waited for.
@@ -124,7 +125,7 @@ template <int NCOL, int MODE>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, int row, uint8_t* stage,
                                                    int stage_bytes, const void* tmap, int col0, int row0_coord,
                                                    int slab_coord, int3 ext, bool have_o, bool leader,
-                                                   const int* abort_flag, unsigned* status) {
+                                                   const int* abort_flag, unsigned* status, int bar_id = 2) {
     constexpr bool F32 = MODE == kOutF32;
     constexpr int BOX_COLS = F32 ? 32 : 64;
     constexpr int CHUNKS_PER_BOX = BOX_COLS / 32;
@@ -173,7 +174,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_col, float inv, in
             }
         }
         fence_proxy_async_smem();
-        named_barrier_sync(2, 128);
+        named_barrier_sync(bar_id, 128);
         const int c0 = col0 + bx * BOX_COLS;
         if (leader && *abort_flag == 0 &&
             FMHA_IN_BOUNDS(c0 >= 0 && c0 % BOX_COLS == 0 && c0 + BOX_COLS <= ext.x && row0_coord >= 0 &&

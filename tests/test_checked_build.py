@@ -79,7 +79,7 @@ def test_checked_build_reports_a_failed_check():
 
 
 SUITES = ["tests/test_parity.py", "tests/test_kernel_paths.py", "tests/test_sink.py", "tests/test_host_entry.py",
-          "tests/test_segments.py", "tests/test_nvfp4.py",
+          "tests/test_segments.py", "tests/test_nvfp4.py", "tests/test_pair_kernel.py",
           "tests/test_zz_no_alloc.py"]
 
 

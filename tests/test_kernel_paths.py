@@ -1,9 +1,12 @@
 """GPU parity of each kernel family on shapes the automatic choice would send
 to the other one: the decode kernel (mma.sync, 8/16 query rows per block) and
-the 128-row tensor-core kernel (tcgen05 + TMEM), both against the fp64 oracle.
-The row-tile kernel's P V product runs in the TS form by default (P written
-over S in tensor memory, read from there as the MMA's A operand); path 3
-forces the SS form (P through shared memory), and both are checked.
+the 128-row tensor-core kernels (tcgen05 + TMEM), all against the fp64 oracle.
+Path 2 forces the tensor-core kernels, with two row tiles per block where that
+kernel applies (hd 64/128, more than 128 rows per KV head); path 4 forces one
+row tile per block.  The row-tile kernel's P V product runs in the TS form by
+default (P written over S in tensor memory, read from there as the MMA's A
+operand); path 3 forces the SS form (P through shared memory), and both are
+checked.
 """
 import numpy as np
 import pytest
@@ -46,7 +49,8 @@ def path():
     binding.fmha_set_kernel_path(0)
 
 
-@pytest.mark.parametrize("which", [1, 2, 3], ids=["decode_kernel", "tensor_core_kernel_ts", "tensor_core_kernel_ss"])
+@pytest.mark.parametrize("which", [1, 2, 3, 4],
+                         ids=["decode_kernel", "tensor_core_kernels", "tensor_core_kernel_ss", "tensor_core_kernel_ts"])
 @pytest.mark.parametrize("w", SHAPES, ids=[w.name for w in SHAPES])
 def test_kernel_family_matches_oracle(w, which, path):
     path(which)
@@ -71,10 +75,10 @@ TS_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("which", [2, 3], ids=["ts", "ss"])
+@pytest.mark.parametrize("which", [4, 3], ids=["ts", "ss"])
 @pytest.mark.parametrize("w", TS_SHAPES, ids=[w.name for w in TS_SHAPES])
 def test_pv_forms_match_oracle(w, which, path):
-    """Row-tile kernel forced, in the TS form (path 2) and the SS form (path 3),
+    """Row-tile kernel forced, in the TS form (path 4) and the SS form (path 3),
     against the oracle."""
     path(which)
     (q, k, v), (qd, kd, vd) = device_inputs(w, seed=12)
