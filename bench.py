@@ -20,10 +20,11 @@ page-locked memory, the forward, and the D2H copies of O and LSE; steps
 alternate between two streams), ``clocks``
 (nvidia-smi sampled during the timed region), ``gpu_launches`` and
 ``secondary`` (the single-head decode -- launch-latency bound, read its
-``us_per_step`` --, the GQA sliding-window decode and the causal prefill, each
-with its own roofline figures, as ``fmha_fwd`` plans them; for the GQA decode also
-``split_512``: the same workload split literally into 512-key chunks with
-``fmha_fwd_splitkv`` + ``fmha_merge``).
+``us_per_step`` --, the GQA sliding-window decode, the causal prefill and a GQA
+short prefill (T 128, group 8, hd 128, 4096 keys: compute-bound, read its
+``frac_bf16_peak``), each with its own roofline figures, as ``fmha_fwd`` plans
+them; for the GQA decode also ``split_512``: the same workload split literally
+into 512-key chunks with ``fmha_fwd_splitkv`` + ``fmha_merge``).
 
 ``--impl reference`` times the fp64 oracle on the host cores instead (the only
 reference implementation this project has), on the same workload and metric.
@@ -580,7 +581,8 @@ def main():
 
     secondary = {}
     if not args.no_secondary:
-        for name, chunk in (("single_head_decode", 0), ("gqa_swa_decode", 512), ("causal_prefill", 0)):
+        for name, chunk in (("single_head_decode", 0), ("gqa_swa_decode", 512), ("causal_prefill", 0),
+                            ("gqa_prefill", 0)):
             w2 = inputs.WORKLOADS[name]
             st = max(20, min(args.steps, 400))
             r2 = run_workload(binding, w2, st, 3, stream, dist)

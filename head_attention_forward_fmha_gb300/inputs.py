@@ -62,6 +62,11 @@ WORKLOADS = {
     "mqa_decode_vconst": Workload("mqa_decode_vconst", 16, 128, 1, 1, 512, 512, v_const_row=True),
     "gqa_swa_decode": Workload("gqa_swa_decode", 32, 64, 8, 1, 8192, 128, window=4096, kv_chunk=512),
     "causal_prefill": Workload("causal_prefill", 8, 32, 32, 128, 512, 256, causal=True),
+    # Not one of the listed configurations: a GQA short prefill (T = 128, eight
+    # query heads per KV head, 4096 cached keys, bottom-right causal), the
+    # compute-bound end of the path (its FLOPs take 2x its bytes' time at the
+    # peaks), where the two-row-tile tensor-core kernel runs.
+    "gqa_prefill": Workload("gqa_prefill", 4, 64, 8, 128, 4096, 128, causal=True),
 }
 
 SWEEP_HD = (64, 128, 256, 512)

@@ -187,6 +187,31 @@ def test_sweep_full_size_sampled_rows(w):
     torch.cuda.empty_cache()
 
 
+def test_gqa_prefill_full_size_sampled_rows():
+    """The GQA short prefill bench.py times (two-row-tile kernel) at full size:
+    48 sampled rows plus every row of four whole (batch, head) slabs against
+    the oracle, all three tolerances."""
+    w = inputs.WORKLOADS["gqa_prefill"]
+    n, _, kern = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal,
+                                       with_kernel=True)
+    assert kern == "fwd_tc_pair", kern
+    qd, kd, vd = inputs.make_inputs(w, seed=9, device="cuda")
+    o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, causal=True)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    slabs = _sweep_slabs(w, 4, seed=9)
+    slab_rows = np.concatenate([(b * w.n_h + h) * w.T + np.arange(w.T, dtype=np.int64) for b, h in slabs])
+    rows = np.union1d(inputs.sample_rows(w, 48, seed=9), slab_rows)
+    o_ref, lse_ref = oracle.attention_rows(to_np_bits(qd), to_np_bits(kd), to_np_bits(vd), rows, w.scale,
+                                           causal=True)
+    idx = torch.from_numpy(rows).cuda()
+    og = o.reshape(-1, w.hd)[idx]
+    compare(og, lse.reshape(-1)[idx], o_ref, lse_ref, w.name)
+    pos = np.searchsorted(rows, slab_rows)
+    og_slabs = og[torch.from_numpy(pos).cuda()].reshape(1, len(slabs), w.T, w.hd)
+    cosine_per_head(og_slabs, o_ref[pos].reshape(1, len(slabs), w.T, w.hd), w.name)
+
+
 CHAIN = [
     # each kernel family, split and unsplit; O of one call is Q of the next
     W("chain_hd512_mqa_split", 2, 128, 1, 1, 512, 512),
