@@ -308,7 +308,7 @@ def measure_kernel_only(binding, w, sets, stream, steps):
         return out
     # The same kernels in the same configuration as fmha_fwd: its hd-512
     # tensor-core path keeps fp16 partials (FMHA_PARTS_F16), the others fp32.
-    f16 = kernel == "fwd_tc_wide"
+    f16 = kernel == "fwd_tc_wide" and w.hd == 512
     out["parts_format"] = "f16" if f16 else "f32"
     parts = []
     for (q, k, v, o, lse) in sets:
