@@ -164,9 +164,9 @@ int sm_count() {
 // head with at least tc_min_rows(hd) query rows goes to the tensor-core
 // kernels: 64 rows at hd <= 128, 32 rows at hd 256 and 512, where the decode
 // kernel's CUDA-core-side work per key grows with hd (measured on the MHA shape
-// sweep).  At hd 128 a KV head with more than 128 rows may also take the
-// two-row-tile kernel (two tiles per block sharing each K/V tile); the planner
-// picks whichever of the two has the lower estimated time.
+// sweep).  At hd 64 and 128 a KV head with more than 128 rows may also take
+// the two-row-tile kernel (two tiles per block sharing each K/V tile); the
+// planner picks whichever of the two has the lower estimated time.
 int tc_min_rows(int hd) { return hd >= 256 ? 32 : 64; }
 // 0 auto, 1 decode kernel, 2 tensor-core kernels (two row tiles per block
 // where the shape allows), 3 tensor-core kernels with the row-tile kernel's
@@ -196,12 +196,12 @@ KernelShape kernel_shape(const Problem& p, Path path) {
 // block ~52 GB/s (96 KB of K/V in flight, ~1.9 us per ring-slot round trip);
 // at hd <= 128 a row-tile block also needs tile_us_per_128_keys of MMAs and
 // softmax per 128 keys, and a two-row-tile block pair_us_per_128_keys for its
-// two tiles (GQA prefill hd 128, T 128: 80.8 us with one row tile per block
-// and 63.0 us with two, s_k 4096).
+// two tiles (GQA prefill T 128, s_k 4096: 80.8 us with one row tile per block
+// and 63.0 us with two at hd 128, 71.5 and 60.5 us at hd 64).
 // The two halves of an hd-512 row tile read the same K, the second from L2,
 // so DRAM serves K and V once per pair of blocks.  At hd 512, s_k 32768
 // (128 row-tile halves) seven chunks measured 891 us against 962 us for one.
-double pair_us_per_128_keys(int) { return 1.9; }
+double pair_us_per_128_keys(int hd) { return hd == 64 ? 1.85 : 1.9; }
 double tile_us_per_128_keys(int hd) { return hd == 64 ? 1.1 : 1.25; }
 
 double tc_split_cost(const Problem& p, const KernelShape& ks, Path path, long long units, long long sms,

@@ -81,9 +81,10 @@ cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream);
 // per half of the head dim of O.
 int tc_wide_kv_tile();
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
-// Two 128-row tiles per thread block (tc_pair_kernel.cu), hd 128: for KV heads
-// with more than 128 query rows; the same Q, O, K and V maps as launch_tc
-// (K/V boxes of tc_pair_kv_tile() keys); bf16 O or fp32 partials, no NVFP4.
+// Two 128-row tiles per thread block (tc_pair_kernel.cu), hd 64 and 128: for
+// KV heads with more than 128 query rows; the same Q, O, K and V maps as
+// launch_tc (K/V boxes of tc_pair_kv_tile() keys); bf16 O or fp32 partials, no
+// NVFP4.
 bool tc_pair_supports(int hd);
 int tc_pair_kv_tile();
 cudaError_t launch_tc_pair(const TcLaunch& L, cudaStream_t stream);

@@ -1,20 +1,22 @@
 // tc_pair_kernel.cu -- attention forward for two 128-row query tiles per
-// thread block on the tcgen05 tensor cores (sm_103a), hd 128.
+// thread block on the tcgen05 tensor cores (sm_103a), hd 64 and 128.
 //
 // When a KV head has more than 128 query rows (a GQA prefill: group x T >
 // 128), one thread block takes two row tiles, A and B, of the same KV head and
 // KV chunk.  Both use every K and V tile the block loads (128 keys each), and
 // two softmax warpgroups, one per row tile, run side by side:
 //   S_t(j)  = Q_t K_j^T                    per row tile t: M = 128 rows, N = 128 keys
-//   O^T    += V_j^T [P_A(j); P_B(j)]^T     once for both tiles: M = hd = 128,
-//                                          N = 256 rows, K = 128 keys
+//   O^T    += V_j^T [P_A(j); P_B(j)]^T     once for both tiles: M = hd (64 or
+//                                          128), N = 256 rows, K = 128 keys
 // The P V product runs transposed so that one MMA instruction covers both
 // row tiles (N = 256): on this GPU a tcgen05.mma of N <= 128 costs about as
 // much as one of N = 256, and P V, with V as the MN-major operand, is the
 // dearer of the two products.  A is V itself (MN-major, as it lies in
 // memory), B is P (K-major, rows of 128 keys), written to shared memory by
-// the softmax.  Tensor memory: S_A, S_B (128 columns each) and O^T (lanes =
-// head-dim index, 256 columns = the two tiles' rows).
+// the softmax.  Tensor memory: S_A, S_B (128 columns each) and O^T (256
+// columns = the two tiles' rows; head-dim index d in lane d at hd 128, and at
+// hd 64, an M = 64 accumulator, in lane (d / 16) * 32 + d % 16: the first 16
+// lanes of each 32-lane quarter, as measured on this GPU).
 //
 // The FA2 online softmax (commit e4ee9fd of the nvfp4-megamoe-kernel pages,
 // multi-tile C API part), the lazy rescale and the bf16-rounded divisor are
@@ -23,7 +25,8 @@
 //
 // Warp roles (12 warps):
 //   warp 0      TMA producer: both Q tiles (once), then K_0 and, per KV tile
-//               j, K_{j+1} and V_j through a ring of three 32 KB slots
+//               j, K_{j+1} and V_j through a ring of K/V tiles (three 32 KB
+//               slots at hd 128, eight 16 KB slots at hd 64)
 //   warp 1      TMEM owner and MMA issuer (one elected lane):
 //               QK_A(0) QK_B(0) | QK_A(j+1) QK_B(j+1) PV(j) | ...
 //   warps 2, 3  idle (keep the softmax warps aligned to TMEM lane quarters)
@@ -50,7 +53,7 @@ namespace {
 
 template <int HD>
 struct PCfg {
-    static_assert(HD == 128, "O^T uses one TMEM lane per head-dim index (M = 128)");
+    static_assert(HD == 64 || HD == 128, "O^T is an M = hd accumulator");
     static constexpr int BM = 128;                  // query rows per row tile
     static constexpr int BN = 128;                  // keys per KV tile
     static constexpr int NB = HD / 64;              // 64-column (128-byte) boxes of Q, K, V
@@ -58,7 +61,7 @@ struct PCfg {
     static constexpr int P_BYTES = 2 * BM * BN * 2; // P of both tiles: BN / 64 groups of 256 rows x 128 bytes
     static constexpr int P_GROUP = 2 * BM * 128;    // one 64-key group of P
     static constexpr int KV_TILE = BN * HD * 2;     // one K or V tile
-    static constexpr int NSLOT = 3;                 // K/V ring slots
+    static constexpr int NSLOT = HD == 64 ? 8 : 3;  // K/V ring slots
     static constexpr int THREADS = 384;
     static constexpr int OT_COL = 2 * BN;           // TMEM: S_A at 0, S_B at BN, O^T at 2 BN
     static constexpr int TMEM_COLS = 512;
@@ -353,7 +356,10 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             const int bar_id = 2 + t;
             const int quarter = warp & 3;
             const int row = quarter * 32 + lane;  // TMEM lane of S_t and row within the tile
-            const int hdi = quarter * 32 + lane;  // TMEM lane of O^T: head-dim index
+            // head-dim index of this thread's TMEM lane of O^T (at hd 64 only the
+            // first 16 lanes of each quarter hold O^T)
+            const int hdi = HD == 128 ? quarter * 32 + lane : quarter * 16 + lane;
+            const bool hd_lane = HD == 128 || lane < 16;
             const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
             const int r_tile = rb + t * BM;
             const int grow = r_tile + row;
@@ -434,7 +440,7 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             uint8_t* stage = t == 0 ? sq : sp;
             if (!a.to_partials) {
                 // bf16 boxes of 64 columns x 128 rows (128-byte rows, swizzled)
-                uint8_t* col = stage + (hdi >> 6) * 16384 + (hdi & 7) * 2;
+                uint8_t* col = stage + ((hdi >> 6) & (HD / 64 - 1)) * 16384 + (hdi & 7) * 2;
                 const int chunk = (hdi & 63) >> 3;
 #pragma unroll 1
                 for (int c = 0; c < BM / 32; ++c) {
@@ -446,16 +452,18 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = 0.f;
                     }
+                    if (hd_lane) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int r = c * 32 + i;
-                        *reinterpret_cast<__nv_bfloat16*>(col + r * 128 + ((chunk ^ (r & 7)) << 4)) =
-                            __float2bfloat16_rn(ov[i] * rowv[t * BM + r]);
+                        for (int i = 0; i < 32; ++i) {
+                            const int r = c * 32 + i;
+                            *reinterpret_cast<__nv_bfloat16*>(col + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+                                __float2bfloat16_rn(ov[i] * rowv[t * BM + r]);
+                        }
                     }
                 }
             } else {
                 // fp32 boxes of 32 columns x 128 rows
-                uint8_t* col = stage + (hdi >> 5) * 16384 + (hdi & 3) * 4;
+                uint8_t* col = stage + ((hdi >> 5) & (HD / 32 - 1)) * 16384 + (hdi & 3) * 4;
                 const int chunk = (hdi & 31) >> 2;
 #pragma unroll 1
                 for (int c = 0; c < BM / 32; ++c) {
@@ -467,10 +475,13 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = 0.f;
                     }
+                    if (hd_lane) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int r = c * 32 + i;
-                        *reinterpret_cast<float*>(col + r * 128 + ((chunk ^ (r & 7)) << 4)) = ov[i] * rowv[t * BM + r];
+                        for (int i = 0; i < 32; ++i) {
+                            const int r = c * 32 + i;
+                            *reinterpret_cast<float*>(col + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+                                ov[i] * rowv[t * BM + r];
+                        }
                     }
                 }
             }
@@ -553,12 +564,14 @@ cudaError_t launch_pair_t(const TcLaunch& L, cudaStream_t stream) {
 
 }  // namespace
 
-bool tc_pair_supports(int hd) { return hd == 128; }
+bool tc_pair_supports(int hd) { return hd == 64 || hd == 128; }
 int tc_pair_kv_tile() { return PCfg<128>::BN; }
 
 cudaError_t launch_tc_pair(const TcLaunch& L, cudaStream_t stream) {
-    if (L.p.hd != 128 || (L.fp4.codes && !L.to_partials)) return cudaErrorInvalidValue;
-    return (L.sink && !L.to_partials) ? launch_pair_t<128, kEpiSink>(L, stream) : launch_pair_t<128, kEpiBf16>(L, stream);
+    if (!tc_pair_supports(L.p.hd) || (L.fp4.codes && !L.to_partials)) return cudaErrorInvalidValue;
+    const bool sink = L.sink && !L.to_partials;
+    if (L.p.hd == 64) return sink ? launch_pair_t<64, kEpiSink>(L, stream) : launch_pair_t<64, kEpiBf16>(L, stream);
+    return sink ? launch_pair_t<128, kEpiSink>(L, stream) : launch_pair_t<128, kEpiBf16>(L, stream);
 }
 
 }  // namespace fmha

@@ -108,7 +108,8 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * *kv_chunk and the kernel family in *kernel (1 = decode kernel, 2 =
  * tensor-core kernel, one 128-row tile per thread block, 3 = tensor-core
  * kernel for hd 512, 4 = tensor-core kernel with two 128-row tiles per thread
- * block, hd 128; fmha_fwd_nvfp4 runs kernel 2 there, with the same chunks);
+ * block, hd 64 and 128; fmha_fwd_nvfp4 runs kernel 2 there, with the same
+ * chunks);
  * either pointer may be NULL.  Pure host arithmetic apart from reading the current device's SM
  * count; negative FMHA_ERR_* code on invalid shapes.
  */
@@ -318,11 +319,11 @@ int fmha_selftest_bounds_check(fmha_stream_t stream);
  * Kernel-family selection for every later call in the process: 0 = automatic
  * (default: the 128-row tensor-core kernels when a KV head has at least 64
  * query rows at hd <= 128, or 32 at hd 256 and 512, else the decode kernel;
- * at hd 128 with more than 128 rows per KV head, one or two row tiles per
- * thread block, whichever the planner estimates faster), 1 = always the
+ * at hd 64 and 128 with more than 128 rows per KV head, one or two row tiles
+ * per thread block, whichever the planner estimates faster), 1 = always the
  * decode kernel, 2 = always the tensor-core kernels, with two row tiles per
- * thread block wherever that kernel applies (hd 128, more than 128 rows per KV
- * head), 3 = always the tensor-core kernels, one row tile per thread
+ * thread block wherever that kernel applies (hd 64 and 128, more than 128 rows
+ * per KV head), 3 = always the tensor-core kernels, one row tile per thread
  * block, and the row-tile kernel (hd <= 256) with its P V product in the "SS"
  * form (P staged in shared memory) instead of the default "TS" form (P
  * written over S in tensor memory and read from there as the MMA's A operand;

@@ -1,9 +1,10 @@
 """GPU parity of the two-row-tile tensor-core kernel (two 128-row query tiles
 per thread block sharing every K/V tile, one softmax warpgroup per tile, P V
-computed transposed for both tiles at once; hd 128) against the fp64 oracle.
+computed transposed for both tiles at once; hd 64 and 128) against the fp64
+oracle.
 
-Path 2 forces it wherever it applies (hd 128, more than 128 query rows per KV
-head); the shapes cover GQA prefill, causal and window masks, row counts that
+Path 2 forces it wherever it applies (hd 64 or 128, more than 128 query rows per
+KV head); the shapes cover GQA prefill, causal and window masks, row counts that
 leave the last block with one row tile or a partial second tile, no key at
 all, T > s_k, long KV ranges, split-KV partials and the attention sink.  The
 NVFP4 output of such a shape runs the one-row-tile kernel (checked here too).
@@ -33,6 +34,12 @@ PAIR_SHAPES = [
     W("p9_long_sk", 1, 8, 1, 32, 5000, 128, causal=True),                        # 40 KV tiles
     W("p10_sharp_softmax", 1, 16, 2, 128, 2048, 128, k_mult=3.0),               # many rescales
     W("p11_window_only_hd128", 1, 4, 1, 128, 3000, 128, window=700),
+    # hd 64: O^T is an M = 64 accumulator (the first 16 lanes of each TMEM quarter)
+    W("p12_gqa8_T128_causal_hd64", 2, 16, 2, 128, 700, 64, causal=True),
+    W("p13_R300_ragged_hd64", 1, 3, 1, 100, 333, 64),
+    W("p14_window_causal_hd64", 1, 8, 2, 64, 900, 64, window=333, causal=True),
+    W("p15_sharp_softmax_hd64", 1, 16, 2, 128, 2048, 64, k_mult=3.0),
+    W("p16_no_key_hd64", 1, 4, 1, 70, 0, 64),
 ]
 
 
@@ -61,11 +68,10 @@ def test_pair_kernel_matches_oracle(w, path):
         cosine_per_head(o, o_ref, w.name)
 
 
-@pytest.mark.parametrize("chunk", [256, 384, 1000])
-def test_pair_kernel_partials(chunk, path):
+@pytest.mark.parametrize("hd,chunk", [(128, 256), (128, 384), (128, 1000), (64, 256), (64, 640)])
+def test_pair_kernel_partials(hd, chunk, path):
     """Split-KV partials of the pair kernel (fp32) and their merge."""
     path(2)
-    hd = 128
     w = W("pair_split", 1, 8, 2, 64, 1500, hd, window=1100, causal=True)
     assert _plan_kernel(w) == "fwd_tc_pair"
     (q, k, v), (qd, kd, vd) = device_inputs(w, seed=22)
@@ -81,9 +87,10 @@ def test_pair_kernel_partials(chunk, path):
     cosine_per_head(o, o_ref, "pair merged hd %d chunk %d" % (hd, chunk))
 
 
-def test_pair_kernel_sink(path):
+@pytest.mark.parametrize("hd", [64, 128])
+def test_pair_kernel_sink(hd, path):
     path(2)
-    w = W("pair_sink", 2, 16, 2, 32, 600, 128, causal=True)
+    w = W("pair_sink", 2, 16, 2, 32, 600, hd, causal=True)
     assert _plan_kernel(w) == "fwd_tc_pair"
     (q, k, v), (qd, kd, vd) = device_inputs(w, seed=23)
     g = torch.Generator().manual_seed(7)

@@ -13,7 +13,7 @@ KV_TILE = {  # keys per tile of each kernel family and head dim
     "decode_splitkv": {64: 64, 128: 64, 256: 32, 512: 32},
     "fwd_tc": {64: 128, 128: 128, 256: 64},
     "fwd_tc_wide": {512: 128},
-    "fwd_tc_pair": {128: 128},
+    "fwd_tc_pair": {64: 128, 128: 128},
 }
 
 
@@ -28,8 +28,8 @@ def expected_families(n_h, n_kv_h, T, hd):
     if rows >= (64 if hd <= 128 else 32):
         if hd == 512:
             return {"fwd_tc_wide"}
-        # more than one 128-row tile per KV head at hd 128: one or two tiles per block
-        return {"fwd_tc", "fwd_tc_pair"} if rows > 128 and hd == 128 else {"fwd_tc"}
+        # more than one 128-row tile per KV head at hd <= 128: one or two tiles per block
+        return {"fwd_tc", "fwd_tc_pair"} if rows > 128 and hd <= 128 else {"fwd_tc"}
     return {"decode_splitkv"}
 
 
@@ -69,9 +69,9 @@ def test_forced_families():
         binding.fmha_set_kernel_path(2)
         assert binding.fmha_fwd_plan(2, 8, 8, 1, 4096, 128, with_kernel=True)[2] == "fwd_tc"
         assert binding.fmha_fwd_plan(2, 8, 8, 1, 4096, 512, with_kernel=True)[2] == "fwd_tc_wide"
-        # two row tiles per block wherever that kernel applies (hd 128, > 128 rows per KV head)
+        # two row tiles per block wherever that kernel applies (hd 64 / 128, > 128 rows per KV head)
         assert binding.fmha_fwd_plan(2, 64, 8, 128, 4096, 128, with_kernel=True)[2] == "fwd_tc_pair"
-        assert binding.fmha_fwd_plan(2, 64, 8, 32, 4096, 64, with_kernel=True)[2] == "fwd_tc"     # hd 64
+        assert binding.fmha_fwd_plan(2, 64, 8, 32, 4096, 64, with_kernel=True)[2] == "fwd_tc_pair"
         assert binding.fmha_fwd_plan(2, 64, 8, 16, 4096, 128, with_kernel=True)[2] == "fwd_tc"    # 128 rows
         assert binding.fmha_fwd_plan(2, 64, 8, 128, 4096, 256, with_kernel=True)[2] == "fwd_tc"   # hd 256
         binding.fmha_set_kernel_path(4)
