@@ -21,15 +21,18 @@ W = inputs.Workload
 
 # Shapes that fmha_fwd splits, so the scratch array is really used: a GQA
 # sliding-window decode with few KV heads (decode kernel, fp32 partials), an
-# MQA decode with many cached keys (tensor-core kernel, fp32 partials) and the
+# MQA decode with many cached keys (tensor-core kernel, fp32 partials), the
 # MQA decode at hd 512 (hd-512 tensor-core kernel, fp16 partials with range
-# factors), whose results are also checked against the fp64 oracle.
+# factors) and two GQA prefills (two-row-tile kernel, fp32 partials, hd 128
+# and 64); the hd-512 and hd-64 ones are also checked against the fp64 oracle.
 SPLIT_SHAPES = [
     W("gqa_swa_decode_b4", 4, 64, 8, 1, 8192, 128, window=4096),
     W("mqa_G128_hd128_long", 2, 128, 1, 1, 4096, 128),
     W("mqa_decode_hd512", 16, 128, 1, 1, 512, 512),
+    W("gqa_prefill_pair_hd128", 1, 64, 8, 128, 4096, 128, causal=True),
+    W("gqa_pair_hd64_long", 1, 32, 2, 64, 8192, 64),
 ]
-ORACLE_CHECKED = {"mqa_decode_hd512"}
+ORACLE_CHECKED = {"mqa_decode_hd512", "gqa_pair_hd64_long"}
 
 
 def _plan(w):
