@@ -196,12 +196,12 @@ KernelShape kernel_shape(const Problem& p, Path path) {
 // block ~52 GB/s (96 KB of K/V in flight, ~1.9 us per ring-slot round trip);
 // at hd <= 128 a row-tile block also needs tile_us_per_128_keys of MMAs and
 // softmax per 128 keys, and a two-row-tile block pair_us_per_128_keys for its
-// two tiles (GQA prefill T 128, s_k 4096: 80.8 us with one row tile per block
-// and 63.0 us with two at hd 128, 71.5 and 60.5 us at hd 64).
+// two tiles (GQA prefill T 128, s_k 4096: 80.7 us with one row tile per block
+// and 64.9 us with two at hd 128, 71.5 and 64.3 us at hd 64).
 // The two halves of an hd-512 row tile read the same K, the second from L2,
 // so DRAM serves K and V once per pair of blocks.  At hd 512, s_k 32768
 // (128 row-tile halves) seven chunks measured 891 us against 962 us for one.
-double pair_us_per_128_keys(int hd) { return hd == 64 ? 1.85 : 1.9; }
+double pair_us_per_128_keys(int) { return 1.95; }
 double tile_us_per_128_keys(int hd) { return hd == 64 ? 1.1 : 1.25; }
 
 double tc_split_cost(const Problem& p, const KernelShape& ks, Path path, long long units, long long sms,

@@ -23,15 +23,16 @@
 // those of tc_kernel.cu; with O transposed, a rescale of row r scales column
 // r of O^T, which all four warps of the row's tile take part in.
 //
-// Warp roles (12 warps):
+// Warp roles (10 warps):
 //   warp 0      TMA producer: both Q tiles (once), then K_0 and, per KV tile
 //               j, K_{j+1} and V_j through a ring of K/V tiles (three 32 KB
 //               slots at hd 128, eight 16 KB slots at hd 64)
 //   warp 1      TMEM owner and MMA issuer (one elected lane):
 //               QK_A(0) QK_B(0) | QK_A(j+1) QK_B(j+1) PV(j) | ...
-//   warps 2, 3  idle (keep the softmax warps aligned to TMEM lane quarters)
-//   warps 4..7  softmax and epilogue of row tile A (one query row per thread)
-//   warps 8..11 softmax and epilogue of row tile B
+//   warps 2..5  softmax and epilogue of row tile A (one query row per thread;
+//               warp w reaches TMEM lane quarter w % 4, so the four warps of a
+//               tile cover quarters 2, 3, 0, 1)
+//   warps 6..9  softmax and epilogue of row tile B
 // A softmax warpgroup frees its S buffer as soon as it has loaded S_t(j), so
 // QK_t(j+1) runs while it computes P_t(j); it writes P_t(j) once PV(j-1) has
 // read the P buffer.  Both warpgroups run one copy of the softmax code (the
@@ -62,14 +63,14 @@ struct PCfg {
     static constexpr int P_GROUP = 2 * BM * 128;    // one 64-key group of P
     static constexpr int KV_TILE = BN * HD * 2;     // one K or V tile
     static constexpr int NSLOT = HD == 64 ? 8 : 3;  // K/V ring slots
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 320;
     static constexpr int OT_COL = 2 * BN;           // TMEM: S_A at 0, S_B at BN, O^T at 2 BN
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;                 // Q_A, then Q_B
     static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_RING = OFF_P + P_BYTES;
     static constexpr int OFF_BAR = OFF_RING + NSLOT * KV_TILE;
-    static constexpr int N_BARS = 1 + 2 * NSLOT + 2 + 2 + 1 + 1 + 1;
+    static constexpr int N_BARS = 1 + 2 * NSLOT + 2 + 2 + 1 + 2 + 1;
     static constexpr int OFF_ROWV = OFF_BAR + N_BARS * 8 + 16;  // after the TMEM address and abort flag
     static constexpr int SMEM = 1024 + OFF_ROWV + 2 * BM * 4;
     static_assert(OT_COL + 2 * BM <= TMEM_COLS, "TMEM budget");
@@ -150,8 +151,8 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
     uint64_t* s_full = slot_empty + NSLOT;  // [2] by row tile: S_t(j) in TMEM
     uint64_t* s_free = s_full + 2;          // [2] by row tile: S_t(j) loaded by its softmax warps
     uint64_t* p_ready = s_free + 2;         // P_A(j) and P_B(j) in shared memory
-    uint64_t* o_done = p_ready + 1;         // PV(j) completed: O^T updated, P buffer and V slot free
-    uint64_t* mma_drain = o_done + 1;       // every MMA the issuer launched has completed (exit drain)
+    uint64_t* o_done = p_ready + 1;         // [2] by j & 1: PV(j) completed (O^T updated, its P buffer and V slot free)
+    uint64_t* mma_drain = o_done + 2;       // every MMA the issuer launched has completed (exit drain)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     float* rowv = reinterpret_cast<float*>(smem + C::OFF_ROWV);  // [2][BM]: per-row alpha, then 1 / sum
@@ -232,7 +233,8 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             mbar_init(&s_free[t], 128);
         }
         mbar_init(p_ready, 128 * n_rt);
-        mbar_init(o_done, 1);
+        mbar_init(&o_done[0], 1);
+        mbar_init(&o_done[1], 1);
         mbar_init(mma_drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
                     const uint64_t bd = smem_desc_sw128(p_addr + (kk >> 2) * C::P_GROUP + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16(tmem + C::OT_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(o_done);
+                tc_commit(&o_done[j & 1]);
                 tc_commit(&slot_empty[sv]);
             }
             // Exit drain: whatever the loop issued has completed before TMEM
@@ -348,10 +350,9 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             tc_commit(mma_drain);
             mbar_wait(mma_drain, 0, a.status);
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax / epilogue of row tile t
-        // (one body per row tile, so its TMEM columns and barrier are constants)
-        const int t = (warp >> 2) - 1;
+        const int t = (warp - 2) >> 2;  // 0: warps 2..5, 1: warps 6..9
         if (t < n_rt) {
             const int bar_id = 2 + t;
             const int quarter = warp & 3;
@@ -372,55 +373,64 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             }
             float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
             bool ok = true;
+            // A failed (timed-out) wait must not split a warpgroup: the loop
+            // holds a named barrier, which has no time limit.  So a thread whose
+            // wait gave up stays in the loop with ok = false, skips every later
+            // wait and all work, and still meets its warpgroup at each barrier;
+            // ok is made warp-uniform before the warp-collective TMEM accesses.
             for (int j = 0; j < n_tiles; ++j) {
-                if (!mbar_wait(&s_full[t], j & 1, a.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float x[BN];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v32[32];
-                    tmem_ld32(t_lane + t * BN + c * 32, v32);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&s_free[t]);  // S_t may now be overwritten by QK_t(j + 1)
-                float alpha;
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, a.status));
+                float alpha = 1.f;
                 uint32_t pk[BN / 2];
-                softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
-                // PV(j - 1) has read the P buffer and updated O^T
-                if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, a.status)) {
-                    ok = false;
-                    break;
+                if (ok) {
+                    tc_fence_after();
+                    float x[BN];
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float v32[32];
+                        tmem_ld32(t_lane + t * BN + c * 32, v32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[c * 32 + i] = v32[i];
+                    }
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&s_free[t]);  // S_t may now be overwritten by QK_t(j + 1)
+                    softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
+                    // PV(j - 1) has read the P buffer and updated O^T (each
+                    // o_done barrier has at most one phase outstanding: PV(j)
+                    // needs this step's P)
+                    if (j > 0) ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status);
                 }
                 // Lazy rescale: column r of O^T (this tile's row r) times alpha_r,
                 // by the four warps that own O^T's lanes.
-                if (j > 0 && named_barrier_or(bar_id, 128, alpha != 1.f)) {
-                    rowv[t * BM + row] = alpha;
+                if (j > 0 && named_barrier_or(bar_id, 128, ok && alpha != 1.f)) {
+                    ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-collective
+                    rowv[t * BM + row] = ok ? alpha : 1.f;
                     named_barrier_sync(bar_id, 128);
-                    tc_fence_after();
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < BM / 32; ++c) {
-                        float ov[32];
-                        tmem_ld32(t_lane + C::OT_COL + t * BM + c * 32, ov);
-                        tmem_wait_ld();
+                        for (int c = 0; c < BM / 32; ++c) {
+                            float ov[32];
+                            tmem_ld32(t_lane + C::OT_COL + t * BM + c * 32, ov);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] *= rowv[t * BM + c * 32 + i];
-                        tmem_st32(t_lane + C::OT_COL + t * BM + c * 32, ov);
+                            for (int i = 0; i < 32; ++i) ov[i] *= rowv[t * BM + c * 32 + i];
+                            tmem_st32(t_lane + C::OT_COL + t * BM + c * 32, ov);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
                 }
-                write_p_row256<BN>(sp, t * BM + row, pk);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(p_ready);
+                if (ok) {
+                    write_p_row256<BN>(sp, t * BM + row, pk);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(p_ready);
+                }
             }
             // -------------------------------------------------------- epilogue
-            if (ok && n_tiles > 0) ok = mbar_wait(o_done, (n_tiles - 1) & 1, a.status);
+            if (ok && n_tiles > 0)
+                ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
             ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
             if (!ok) atomicOr(abort_flag, 1);
             float inv, lse;
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             }
             fence_proxy_async_smem();
             named_barrier_sync(bar_id, 128);
-            if (threadIdx.x == 128 * (t + 1) && *abort_flag == 0) {
+            if (threadIdx.x == 64 + 128 * t && *abort_flag == 0) {
                 const int n_box = a.to_partials ? HD / 32 : HD / 64;
                 const int box_cols = a.to_partials ? 32 : 64;
                 const int slab_c = a.to_partials ? split * (int)(a.rows_total / a.R) + slab : slab;
