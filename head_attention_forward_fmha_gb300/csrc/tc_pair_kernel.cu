@@ -376,10 +376,12 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
             // A failed (timed-out) wait must not split a warpgroup: the loop
             // holds a named barrier, which has no time limit.  So a thread whose
             // wait gave up stays in the loop with ok = false, skips every later
-            // wait and all work, and still meets its warpgroup at each barrier;
-            // ok is made warp-uniform before the warp-collective TMEM accesses.
+            // wait and all work, and still meets its warpgroup at each barrier.
+            // Within a warp the result of a wait is uniform (its lanes test the
+            // barrier word and the timer in the same instructions); warps of the
+            // group can disagree, which the barrier then tolerates.
             for (int j = 0; j < n_tiles; ++j) {
-                ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, a.status));
+                ok = ok && mbar_wait(&s_full[t], j & 1, a.status);
                 float alpha = 1.f;
                 uint32_t pk[BN / 2];
                 if (ok) {
