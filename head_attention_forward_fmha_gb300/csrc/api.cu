@@ -183,7 +183,7 @@ KernelShape kernel_shape(const Problem& p, Path path) {
     if (path == Path::TensorCore) return {kTcRows, tc_kv_tile(p.hd), 1, 1, 256};
     if (path == Path::TensorCorePair) return {2 * kTcRows, tc_pair_kv_tile(), 1, 1, 256};
     if (path == Path::TensorCoreWide) return {kTcRows, tc_wide_kv_tile(), 1, 2, 128};
-    return {decode_rows_per_cta(p.hd, p.R), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2, 1, 256};
+    return {decode_rows_per_cta(p), decode_kv_tile(p.hd), p.hd == 512 ? 1 : 2, 1, 256};
 }
 
 // Estimated time (us) of a tensor-core split into n chunks: waves of blocks

@@ -1,6 +1,6 @@
 // decode_kernel.cu -- split-KV attention forward for few query rows per KV head.
 //
-// One thread block handles RT (8 or 16) query rows that share one KV head
+// One thread block handles RT (8, 16, or 32 at hd 64) query rows that share one KV head
 // (the GQA group of a decode step, or a slice of a short prefill) and one
 // chunk of the KV range.  K and V stream HBM -> shared memory through a
 // multi-stage TMA pipeline (128-byte swizzled boxes of 64 head-dim columns)
@@ -18,6 +18,7 @@
 //
 // Output: bf16 O and fp32 LSE directly, or fp32 partials (O_i, lse_i) of this
 // chunk for the LSE merge (CURRENT_ISSUE.md, "Next steps" item 4).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <atomic>
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
     named_barrier_sync(1, C::NCW * 32);  // Q staged
 
     const uint32_t qs_addr = smem_u32(qs);
-    const uint32_t q_addr = qs_addr + ((lane & 7) + (NB == 2 ? 8 * (lane >> 4) : 0)) * C::Q_STRIDE +
+    const uint32_t q_addr = qs_addr + ((lane & 7) + (NB >= 2 ? 8 * (lane >> 4) : 0)) * C::Q_STRIDE +
                             ((lane >> 3) & 1) * 16;
     const int k_row = 16 * kw + (lane & 15);
     const int k_c8 = lane >> 4;
@@ -236,6 +237,11 @@ __global__ void __launch_bounds__(DCfg<HD, NB>::THREADS)
                 ldsm_x2(qa, bq[0][0], bq[0][1]);
             } else {
                 ldsm_x4(qa, bq[0][0], bq[0][1], bq[1][0], bq[1][1]);
+            }
+            if constexpr (NB == 4) {  // rows 16..31
+                uint32_t qb = qa + 16 * C::Q_STRIDE;
+                if (!FMHA_IN_BOUNDS(qb + 16 <= qs_addr + C::Q_BYTES, kSiteDecLdsmQ, a.status)) qb = qs_addr;
+                ldsm_x4(qb, bq[2][0], bq[2][1], bq[3][0], bq[3][1]);
             }
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sc[nb], a0, a1, a2, a3, bq[nb][0], bq[nb][1]);
@@ -486,13 +492,25 @@ cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
 
 int decode_kv_tile(int hd) { return hd <= 128 ? 64 : 32; }
 
-int decode_rows_per_cta(int hd, int R) { return (R > 8 && hd <= 256) ? 16 : 8; }
+// 32 rows at hd 64 when a KV head has more than 16 and its rows attend at
+// least 16384 keys: each block then reads its K/V chunk for twice the rows
+// (registers still allow two blocks per SM).  Measured on MHA hd 64 T 32:
+// s_k 32768 121.6 -> 110.1 us, but s_k 4096 20.3 -> 23.6 us and s_k 512
+// 7.4 -> 11.0 us, where half as many blocks leave the SMs short of work.
+int decode_rows_per_cta(const Problem& p) {
+    const long long span = p.window > 0 ? std::min<long long>(p.s_k, (long long)p.window + p.T) : p.s_k;
+    if (p.hd == 64 && p.R > 16 && span >= 16384) return 32;
+    return (p.R > 8 && p.hd <= 256) ? 16 : 8;
+}
 
 template <int EPI>
 cudaError_t launch_hd(const DecodeLaunch& L, cudaStream_t stream) {
-    const bool two = decode_rows_per_cta(L.p.hd, L.p.R) == 16;
+    const int rows = decode_rows_per_cta(L.p);
+    const bool two = rows == 16;
     switch (L.p.hd) {
-        case 64: return two ? launch_t<64, 2, EPI>(L, stream) : launch_t<64, 1, EPI>(L, stream);
+        case 64:
+            return rows == 32 ? launch_t<64, 4, EPI>(L, stream)
+                              : two ? launch_t<64, 2, EPI>(L, stream) : launch_t<64, 1, EPI>(L, stream);
         case 128: return two ? launch_t<128, 2, EPI>(L, stream) : launch_t<128, 1, EPI>(L, stream);
         case 256: return two ? launch_t<256, 2, EPI>(L, stream) : launch_t<256, 1, EPI>(L, stream);
         case 512: return launch_t<512, 1, EPI>(L, stream);

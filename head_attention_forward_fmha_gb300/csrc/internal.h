@@ -50,7 +50,7 @@ struct DecodeLaunch {
     unsigned* status;
 };
 int decode_kv_tile(int hd);                  // keys per pipeline stage (TMA box rows)
-int decode_rows_per_cta(int hd, int R);      // query rows per thread block
+int decode_rows_per_cta(const Problem& p);   // query rows per thread block
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 
 // ---- 128-row tensor-core kernel (tc_kernel.cu) ----------------------------

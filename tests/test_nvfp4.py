@@ -61,6 +61,7 @@ SHAPES = [
     W("dec_unsplit_hd128", 2, 8, 2, 1, 300, 128),
     W("dec_split_window", 1, 8, 1, 1, 4096, 128, window=3000),
     W("dec_hd64_T3_window_causal", 2, 6, 3, 3, 150, 64, window=40, causal=True),
+    W("dec_hd64_R48_causal_long", 1, 8, 1, 6, 16500, 64, causal=True),
     W("dec_hd512", 1, 4, 4, 1, 100, 512),
     # row-tile tensor-core kernel, unsplit and split
     W("tc_causal_hd64", 1, 2, 2, 128, 300, 64, causal=True),

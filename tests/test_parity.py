@@ -41,6 +41,11 @@ SMALL = [
     W("s18_hd256_T128_window", 1, 2, 1, 128, 700, 256, window=100, causal=True),
     W("s19_long_sk", 1, 4, 1, 1, 5000, 128),
     W("s20_mqa_G128_hd128", 2, 128, 1, 1, 257, 128),
+    # 32-row decode blocks: hd 64, 17 to 63 rows per KV head, >= 16384 attended keys
+    W("s21_hd64_T32_causal_long", 1, 4, 4, 32, 16400, 64, causal=True),
+    W("s22_hd64_R40_window_long", 1, 8, 2, 10, 20000, 64, window=16380),
+    W("s23_hd64_R24_window_causal", 2, 6, 2, 8, 200, 64, window=50, causal=True),  # 16-row blocks
+    W("s24_hd64_R63_long", 1, 9, 1, 7, 16500, 64),
 ]
 
 
@@ -108,6 +113,7 @@ SPLIT_CASES = [
     (W("sp3", 1, 8, 8, 4, 257, 256, causal=True), 64),
     (W("sp4", 1, 2, 1, 2, 200, 512), 100),
     (W("sp5", 1, 16, 2, 1, 129, 128), 129),
+    (W("sp6_hd64_R32_long", 1, 8, 2, 8, 17000, 64, causal=True), 4096),
 ]
 
 

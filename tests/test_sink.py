@@ -22,6 +22,7 @@ W = inputs.Workload
 SHAPES = [
     W("sink_gqa_decode", 2, 16, 2, 1, 300, 128),
     W("sink_T4_causal_hd64", 2, 8, 8, 4, 70, 64, causal=True),
+    W("sink_hd64_R40_causal_long", 1, 8, 2, 10, 16500, 64, causal=True),
     W("sink_window_hd256", 1, 32, 1, 2, 900, 256, window=300),
     W("sink_prefill_hd256", 2, 4, 4, 128, 256, 256, causal=True),
     W("sink_mqa_hd512_split", 2, 128, 1, 1, 512, 512),
