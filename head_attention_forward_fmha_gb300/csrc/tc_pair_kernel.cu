@@ -9,11 +9,11 @@
 //   O^T    += V_j^T [P_A(j); P_B(j)]^T     once for both tiles: M = hd (64 or
 //                                          128), N = 256 rows, K = 128 keys
 // The P V product runs transposed so that one MMA instruction covers both
-// row tiles (N = 256): on this GPU a tcgen05.mma of N <= 128 costs about as
-// much as one of N = 256, and P V, with V as the MN-major operand, is the
-// dearer of the two products.  A is V itself (MN-major, as it lies in
-// memory), B is P (K-major, rows of 128 keys), written to shared memory by
-// the softmax.  Tensor memory: S_A, S_B (128 columns each) and O^T (256
+// row tiles (N = 256): half the P V instructions, and so fewer operand reads
+// of V and fewer points where the issuing thread must wait, in a kernel whose
+// MMA operands, P writes and K/V loads keep shared memory busy.  A is V itself
+// (MN-major, as it lies in memory), B is P (K-major, rows of 128 keys),
+// written to shared memory by the softmax.  Tensor memory: S_A, S_B (128 columns each) and O^T (256
 // columns = the two tiles' rows; head-dim index d in lane d at hd 128, and at
 // hd 64, an M = 64 accumulator, in lane (d / 16) * 32 + d % 16: the first 16
 // lanes of each 32-lane quarter, as measured on this GPU).
