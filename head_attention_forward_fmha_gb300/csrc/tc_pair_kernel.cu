@@ -41,8 +41,8 @@
 // (GQA prefill hd 128, s_k 4096: 110.7 us against 63.0 us).
 //
 // Measured on GB300 (GQA prefill b4 h64 kv8 T128 hd128 causal): s_k 4096 in
-// 63.0 us (56 % of the bf16 peak) against 80.8 us for one row tile per block;
-// s_k 32768 in 121.7 us (59 %) against 150.2 us.
+// 65 us (54-55 % of the bf16 peak) against 80.7 us for one row tile per block;
+// s_k 32768 in 125.6 us (57 %) against 149.9 us.
 #include <climits>
 #include <atomic>
 #include "internal.h"
