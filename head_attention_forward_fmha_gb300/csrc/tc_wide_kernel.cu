@@ -25,28 +25,35 @@ namespace {
 // QRES = false: Q and K chunks stream through one 8-slot ring (a block with
 // a single KV tile reads Q once either way).  QRES = true (blocks with two or
 // more KV tiles): the 128 KB Q tile is loaded once and stays resident, and
-// only K and V chunks stream through a 6-slot ring; the epilogue then stages
-// O in the Q region.  In both, P goes over S in tensor memory and the P V
-// MMAs read it from there (the TS form), so no shared memory holds P.
+// only K and V chunks stream, two 64-column chunks per ring item (three 32 KB
+// items, one barrier each: a barrier test costs the MMA-issuing thread ~240
+// cycles after N = 128 MMAs, so fewer and larger items keep the tensor pipe
+// fed); the epilogue then stages O in the Q region.  In both, P goes over S
+// in tensor memory and the P V MMAs read it from there (the TS form), so no
+// shared memory holds P.
 template <bool QRES>
 struct WCfgT {
     static constexpr int HD = 512;
     static constexpr int HALF = 256;
     static constexpr int BM = 128;
     static constexpr int BN = 128;
-    static constexpr int SLOT_BYTES = 128 * 128;       // 128 rows x 64 bf16 columns
+    static constexpr int SLOT_BYTES = 128 * 128;       // one chunk: 128 rows x 64 bf16 columns
     static constexpr int Q_CHUNKS = HD / 64;
-    static constexpr int NSLOT = QRES ? 6 : 8;
-    static constexpr int QK_ITEMS = QRES ? Q_CHUNKS : 2 * Q_CHUNKS;  // (Q chunk +) K chunk per column block
-    static constexpr int V_ITEMS = HALF / 64;
+    static constexpr int CPI = QRES ? 2 : 1;           // chunks per ring item
+    static constexpr int ITEM_BYTES = CPI * SLOT_BYTES;
+    static constexpr int NSLOT = QRES ? 3 : 8;         // ring items
+    static constexpr int QK_ITEMS = QRES ? Q_CHUNKS / CPI : 2 * Q_CHUNKS;  // (Q chunk +) K chunk(s) per item
+    static constexpr int V_CHUNKS = HALF / 64;
+    static constexpr int V_ITEMS = V_CHUNKS / CPI;
     static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
-    // The V items of a tile start at an index that is a multiple of V_GROUP,
-    // so each group of V_GROUP items sits in consecutive slots: P V is one MMA
-    // of N = 64 V_GROUP per group and 16 keys (one N = 256 MMA with the 8-slot
-    // ring; two N = 128 MMAs with the 6-slot ring, whose tiles' V chunks may
-    // wrap around the ring between the pairs).
-    static constexpr int V_GROUP = (NSLOT % V_ITEMS == 0) ? V_ITEMS : 2;
-    static_assert(QK_ITEMS % V_GROUP == 0 && NSLOT % V_GROUP == 0 && V_ITEMS % V_GROUP == 0,
+    // P V is one MMA of N = 64 V_GROUP per group of V_GROUP chunks and 16 keys,
+    // the group's chunks one SLOT_BYTES apart: one N = 256 MMA over the four V
+    // items of the 8-slot ring (a tile's V items start at a multiple of 4, so
+    // they never wrap around the ring); two N = 128 MMAs, one per two-chunk
+    // item, with the resident Q.
+    static constexpr int V_GROUP = QRES ? 2 : 4;
+    static constexpr int V_GROUP_ITEMS = V_GROUP / CPI;
+    static_assert(QK_ITEMS % V_GROUP_ITEMS == 0 && NSLOT % V_GROUP_ITEMS == 0 && V_ITEMS % V_GROUP_ITEMS == 0,
                   "V slot groups must be contiguous");
     static constexpr int P_BYTES = 0;  // P lives in tensor memory
     static constexpr int THREADS = 192;
@@ -54,14 +61,14 @@ struct WCfgT {
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;                                   // QRES: resident Q (128 KB)
     static constexpr int OFF_RING = QRES ? Q_CHUNKS * SLOT_BYTES : 0;
-    static constexpr int OFF_P = OFF_RING + NSLOT * SLOT_BYTES;
+    static constexpr int OFF_P = OFF_RING + NSLOT * ITEM_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
     static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging (128 KB)
     static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + 2 + 1 + (QRES ? 1 : 0);
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((QRES ? Q_CHUNKS : NSLOT) * SLOT_BYTES >= BM * HALF * 4, "the epilogue stages fp32 O");
+    static_assert((QRES ? Q_CHUNKS * SLOT_BYTES : NSLOT * ITEM_BYTES) >= BM * HALF * 4, "the epilogue stages fp32 O");
 };
 using WCfg = WCfgT<false>;
 
@@ -145,8 +152,9 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
     // Producer item sequence: QK(0), then for each tile j: QK(j+1) (if any)
     // and V(j) -- the order the MMA warp consumes them in.  Item i -> kind
-    // (0 Q chunk, 1 K chunk, 2 V chunk), tile and 64-column chunk.  With a
-    // resident Q the QK items are K chunks only.
+    // (0 Q chunk, 1 K chunk(s), 2 V chunk(s)), tile and item index c within the
+    // kind (its first 64-column chunk is c * CPI).  With a resident Q the QK
+    // items are K items only.
     const int n_items = n_tiles * C::TILE_ITEMS;
     auto item_of = [&](int i, int& kind, int& tile, int& c) {
         if (i < C::QK_ITEMS) {
@@ -176,18 +184,22 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         const int s = i % C::NSLOT;
         const int key = k_lo + tile * BN;
         const bool in_range = kind == 0 ? (r_begin >= 0 && r_begin < a.R && c >= 0 && c < C::Q_CHUNKS)
-                            : kind == 1 ? (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::Q_CHUNKS)
+                            : kind == 1 ? (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::Q_CHUNKS / C::CPI)
                                         : (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::V_ITEMS);
         if (!FMHA_IN_BOUNDS(in_range && s >= 0 && s < C::NSLOT && slab < (int)gridDim.z, kSiteWideItem, a.status))
             return false;
-        mbar_arrive_expect_tx(&slot_full[s], C::SLOT_BYTES);
-        uint8_t* dst = ring + s * C::SLOT_BYTES;
-        if (kind == 0)
-            tma_load_3d_hint(dst, &tmq, c * 64, r_begin, slab, &slot_full[s], pol_q);
-        else if (kind == 1)
-            tma_load_3d_hint(dst, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
-        else
-            tma_load_3d_hint(dst, &tmv, half * C::HALF + c * 64, key, slab, &slot_full[s], pol_kv);
+        mbar_arrive_expect_tx(&slot_full[s], C::ITEM_BYTES);
+#pragma unroll
+        for (int sub = 0; sub < C::CPI; ++sub) {
+            uint8_t* dst = ring + s * C::ITEM_BYTES + sub * C::SLOT_BYTES;
+            const int ch = c * C::CPI + sub;
+            if (kind == 0)
+                tma_load_3d_hint(dst, &tmq, ch * 64, r_begin, slab, &slot_full[s], pol_q);
+            else if (kind == 1)
+                tma_load_3d_hint(dst, &tmk, ch * 64, key, slab, &slot_full[s], pol_kv);
+            else
+                tma_load_3d_hint(dst, &tmv, half * C::HALF + ch * 64, key, slab, &slot_full[s], pol_kv);
+        }
         return true;
     };
 
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             };
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t d = tmem + (j & 1) * BN;
-                for (int c = 0; c < C::Q_CHUNKS; ++c) {
+                for (int c = 0; c < C::Q_CHUNKS / C::CPI; ++c) {
                     int sq = 0, sk;
                     if (!QRES && !slot_take(sq)) return false;
                     if (!slot_take(sk)) return false;
@@ -275,12 +287,17 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                                         a.status))
                         return false;
                     tc_fence_after();
-                    const uint32_t a_base = QRES ? q_addr + c * C::SLOT_BYTES : ring_addr + sq * C::SLOT_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(ring_addr + sk * C::SLOT_BYTES + kk * 32, 16, 1024);
-                        tc_mma_f16(d, ad, bd, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                    for (int sub = 0; sub < C::CPI; ++sub) {
+                        const int ch = c * C::CPI + sub;  // 64-column chunk of hd
+                        const uint32_t a_base = QRES ? q_addr + ch * C::SLOT_BYTES : ring_addr + sq * C::ITEM_BYTES;
+                        const uint32_t b_base = ring_addr + sk * C::ITEM_BYTES + sub * C::SLOT_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                            tc_mma_f16(d, ad, bd, idesc_s, (ch > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     if (!QRES) tc_commit(&slot_empty[sq]);
                     tc_commit(&slot_empty[sk]);
@@ -297,21 +314,21 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                 for (int c = 0; c < C::V_ITEMS && ok; ++c) {
                     ok = slot_take(sv[c]);
                     if (ok)
-                        ok = FMHA_IN_BOUNDS(sv[c] < C::NSLOT && (c % C::V_GROUP == 0 || sv[c] == sv[c - 1] + 1),
+                        ok = FMHA_IN_BOUNDS(sv[c] < C::NSLOT && (c % C::V_GROUP_ITEMS == 0 || sv[c] == sv[c - 1] + 1),
                                             kSiteWideVSlots, a.status);
                 }
                 if (!ok) break;
                 tc_fence_after();
                 // A: P_j in TMEM over S_j (8 columns = 16 keys per MMA); B: each
-                // group of V_GROUP 64-column V boxes, one slot apart (the
+                // group of V_GROUP 64-column V boxes, one chunk apart (the
                 // descriptor's leading byte offset), into its columns of O.
                 const uint32_t p_col = (j & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
 #pragma unroll
-                    for (int g = 0; g < C::V_ITEMS / C::V_GROUP; ++g) {
+                    for (int g = 0; g < C::V_CHUNKS / C::V_GROUP; ++g) {
                         const uint64_t bd = smem_desc_sw128(
-                            ring_addr + sv[g * C::V_GROUP] * C::SLOT_BYTES + kk * 16 * 128, C::SLOT_BYTES, 1024);
+                            ring_addr + sv[g * C::V_GROUP_ITEMS] * C::ITEM_BYTES + kk * 16 * 128, C::SLOT_BYTES, 1024);
                         tc_mma_f16_ts(tmem + C::O_COL + g * 64 * C::V_GROUP, tmem + p_col + kk * 8, bd, idesc_o,
                                       (j > 0 || kk > 0) ? 1u : 0u);
                     }
