@@ -22,15 +22,16 @@
 namespace fmha {
 namespace {
 
-// QRES = false: Q and K chunks stream through one 8-slot ring (a block with
-// a single KV tile reads Q once either way).  QRES = true (blocks with two or
-// more KV tiles): the 128 KB Q tile is loaded once and stays resident, and
-// only K and V chunks stream, two 64-column chunks per ring item (three 32 KB
-// items, one barrier each: a barrier test costs the MMA-issuing thread ~240
-// cycles after N = 128 MMAs, so fewer and larger items keep the tensor pipe
-// fed); the epilogue then stages O in the Q region.  In both, P goes over S
-// in tensor memory and the P V MMAs read it from there (the TS form), so no
-// shared memory holds P.
+// Every ring item holds two 64-column chunks under one barrier: a barrier
+// test costs the MMA-issuing thread ~240 cycles after N = 128 MMAs, so fewer
+// and larger items keep the tensor pipe fed.  QRES = false: the items are
+// (Q chunk c, K chunk c) pairs, then the V chunks, through a ring of four
+// 32 KB items (a block with a single KV tile reads Q once either way).
+// QRES = true (blocks with two or more KV tiles): the 128 KB Q tile is loaded
+// once and stays resident, and only K and V chunks stream, through three
+// 32 KB items; the epilogue then stages O in the Q region.  In both, P goes
+// over S in tensor memory and the P V MMAs read it from there (the TS form),
+// so no shared memory holds P.
 template <bool QRES>
 struct WCfgT {
     static constexpr int HD = 512;
@@ -39,18 +40,18 @@ struct WCfgT {
     static constexpr int BN = 128;
     static constexpr int SLOT_BYTES = 128 * 128;       // one chunk: 128 rows x 64 bf16 columns
     static constexpr int Q_CHUNKS = HD / 64;
-    static constexpr int CPI = QRES ? 2 : 1;           // chunks per ring item
+    static constexpr int CPI = 2;                      // chunks per ring item
     static constexpr int ITEM_BYTES = CPI * SLOT_BYTES;
-    static constexpr int NSLOT = QRES ? 3 : 8;         // ring items
-    static constexpr int QK_ITEMS = QRES ? Q_CHUNKS / CPI : 2 * Q_CHUNKS;  // (Q chunk +) K chunk(s) per item
+    static constexpr int NSLOT = QRES ? 3 : 4;         // ring items
+    static constexpr int QK_ITEMS = QRES ? Q_CHUNKS / CPI : Q_CHUNKS;  // (K, K) or (Q, K) chunk pairs per tile
     static constexpr int V_CHUNKS = HALF / 64;
     static constexpr int V_ITEMS = V_CHUNKS / CPI;
     static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
     // P V is one MMA of N = 64 V_GROUP per group of V_GROUP chunks and 16 keys,
-    // the group's chunks one SLOT_BYTES apart: one N = 256 MMA over the four V
-    // items of the 8-slot ring (a tile's V items start at a multiple of 4, so
-    // they never wrap around the ring); two N = 128 MMAs, one per two-chunk
-    // item, with the resident Q.
+    // the group's chunks one SLOT_BYTES apart: one N = 256 MMA over the two V
+    // items of the 4-item ring (a tile's V items start at an even index, so
+    // they never wrap around the ring); two N = 128 MMAs, one per item, with
+    // the resident Q.
     static constexpr int V_GROUP = QRES ? 2 : 4;
     static constexpr int V_GROUP_ITEMS = V_GROUP / CPI;
     static_assert(QK_ITEMS % V_GROUP_ITEMS == 0 && NSLOT % V_GROUP_ITEMS == 0 && V_ITEMS % V_GROUP_ITEMS == 0,
@@ -152,23 +153,22 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
     // Producer item sequence: QK(0), then for each tile j: QK(j+1) (if any)
     // and V(j) -- the order the MMA warp consumes them in.  Item i -> kind
-    // (0 Q chunk, 1 K chunk(s), 2 V chunk(s)), tile and item index c within the
-    // kind (its first 64-column chunk is c * CPI).  With a resident Q the QK
-    // items are K items only.
+    // (1 QK item: Q chunk c and K chunk c, or with a resident Q K chunks 2c and
+    // 2c + 1; 2 V item: V chunks 2c and 2c + 1 of this half), tile and c.
     const int n_items = n_tiles * C::TILE_ITEMS;
     auto item_of = [&](int i, int& kind, int& tile, int& c) {
         if (i < C::QK_ITEMS) {
             tile = 0;
-            kind = QRES ? 1 : (i & 1);
-            c = QRES ? i : (i >> 1);
+            kind = 1;
+            c = i;
             return;
         }
         const int r = i - C::QK_ITEMS;
         const int j = r / C::TILE_ITEMS, o = r - j * C::TILE_ITEMS;
         if (j < n_tiles - 1 && o < C::QK_ITEMS) {
             tile = j + 1;
-            kind = QRES ? 1 : (o & 1);
-            c = QRES ? o : (o >> 1);
+            kind = 1;
+            c = o;
         } else {
             tile = j;
             kind = 2;
@@ -183,22 +183,23 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         item_of(i, kind, tile, c);
         const int s = i % C::NSLOT;
         const int key = k_lo + tile * BN;
-        const bool in_range = kind == 0 ? (r_begin >= 0 && r_begin < a.R && c >= 0 && c < C::Q_CHUNKS)
-                            : kind == 1 ? (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::Q_CHUNKS / C::CPI)
-                                        : (key >= 0 && key < k_hi && k_hi <= a.s_k && c >= 0 && c < C::V_ITEMS);
+        const bool key_ok = key >= 0 && key < k_hi && k_hi <= a.s_k;
+        const bool in_range = kind == 1 ? (key_ok && c >= 0 && c < C::QK_ITEMS && (QRES || (r_begin >= 0 && r_begin < a.R)))
+                                        : (key_ok && c >= 0 && c < C::V_ITEMS);
         if (!FMHA_IN_BOUNDS(in_range && s >= 0 && s < C::NSLOT && slab < (int)gridDim.z, kSiteWideItem, a.status))
             return false;
         mbar_arrive_expect_tx(&slot_full[s], C::ITEM_BYTES);
-#pragma unroll
-        for (int sub = 0; sub < C::CPI; ++sub) {
-            uint8_t* dst = ring + s * C::ITEM_BYTES + sub * C::SLOT_BYTES;
-            const int ch = c * C::CPI + sub;
-            if (kind == 0)
-                tma_load_3d_hint(dst, &tmq, ch * 64, r_begin, slab, &slot_full[s], pol_q);
-            else if (kind == 1)
-                tma_load_3d_hint(dst, &tmk, ch * 64, key, slab, &slot_full[s], pol_kv);
-            else
-                tma_load_3d_hint(dst, &tmv, half * C::HALF + ch * 64, key, slab, &slot_full[s], pol_kv);
+        uint8_t* dst = ring + s * C::ITEM_BYTES;
+        if (kind == 2) {
+            tma_load_3d_hint(dst, &tmv, half * C::HALF + 2 * c * 64, key, slab, &slot_full[s], pol_kv);
+            tma_load_3d_hint(dst + C::SLOT_BYTES, &tmv, half * C::HALF + (2 * c + 1) * 64, key, slab, &slot_full[s],
+                             pol_kv);
+        } else if (QRES) {
+            tma_load_3d_hint(dst, &tmk, 2 * c * 64, key, slab, &slot_full[s], pol_kv);
+            tma_load_3d_hint(dst + C::SLOT_BYTES, &tmk, (2 * c + 1) * 64, key, slab, &slot_full[s], pol_kv);
+        } else {
+            tma_load_3d_hint(dst, &tmq, c * 64, r_begin, slab, &slot_full[s], pol_q);
+            tma_load_3d_hint(dst + C::SLOT_BYTES, &tmk, c * 64, key, slab, &slot_full[s], pol_kv);
         }
         return true;
     };
@@ -279,19 +280,18 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             };
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t d = tmem + (j & 1) * BN;
-                for (int c = 0; c < C::Q_CHUNKS / C::CPI; ++c) {
-                    int sq = 0, sk;
-                    if (!QRES && !slot_take(sq)) return false;
+                for (int c = 0; c < C::QK_ITEMS; ++c) {
+                    int sk;
                     if (!slot_take(sk)) return false;
-                    if (!FMHA_IN_BOUNDS(sq >= 0 && sq < C::NSLOT && sk >= 0 && sk < C::NSLOT, kSiteWideQKDesc,
-                                        a.status))
-                        return false;
+                    if (!FMHA_IN_BOUNDS(sk >= 0 && sk < C::NSLOT, kSiteWideQKDesc, a.status)) return false;
                     tc_fence_after();
+                    const uint32_t item_addr = ring_addr + sk * C::ITEM_BYTES;
 #pragma unroll
-                    for (int sub = 0; sub < C::CPI; ++sub) {
-                        const int ch = c * C::CPI + sub;  // 64-column chunk of hd
-                        const uint32_t a_base = QRES ? q_addr + ch * C::SLOT_BYTES : ring_addr + sq * C::ITEM_BYTES;
-                        const uint32_t b_base = ring_addr + sk * C::ITEM_BYTES + sub * C::SLOT_BYTES;
+                    for (int sub = 0; sub < (QRES ? 2 : 1); ++sub) {
+                        const int ch = QRES ? 2 * c + sub : c;  // 64-column chunk of hd
+                        // A: Q chunk ch (resident, or the item's first half); B: its K chunk
+                        const uint32_t a_base = QRES ? q_addr + ch * C::SLOT_BYTES : item_addr;
+                        const uint32_t b_base = QRES ? item_addr + sub * C::SLOT_BYTES : item_addr + C::SLOT_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
@@ -299,7 +299,6 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                             tc_mma_f16(d, ad, bd, idesc_s, (ch > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    if (!QRES) tc_commit(&slot_empty[sq]);
                     tc_commit(&slot_empty[sk]);
                 }
                 tc_commit(&s_full[j & 1]);
@@ -444,7 +443,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         }
         // This half of O -> shared memory (the drained ring) -> TMA store.
         const int pslab = split * (int)(a.rows_total / a.R) + slab;
-        constexpr int kStageBytes = (QRES ? C::Q_CHUNKS : C::NSLOT) * C::SLOT_BYTES;
+        constexpr int kStageBytes = QRES ? C::Q_CHUNKS * C::SLOT_BYTES : C::NSLOT * C::ITEM_BYTES;
         const int3 ext = make_int3(C::HD, a.R, (int)(a.to_partials ? gridDim.y * gridDim.z : gridDim.z));
         if constexpr (EPI == kEpiNvfp4) {
             // quantised in registers and stored per row; rows past the slab's
