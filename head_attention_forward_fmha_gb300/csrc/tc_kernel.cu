@@ -289,8 +289,11 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
                 const int s = j % VST;
                 const int pb = j & 1;
                 if (!FMHA_IN_BOUNDS(s >= 0 && s < VST && pb < 2, kSiteTcVDesc, a.status)) break;
-                if (!mbar_wait(&p_ready[pb], (j >> 1) & 1, a.status)) break;
+                // V_j has usually landed long before P_j: test it first, while the
+                // softmax still works, so that no barrier test (~240 cycles for
+                // this thread) stands between P_j and its MMAs
                 if (!mbar_wait(&v_full[s], (j / VST) & 1, a.status)) break;
+                if (!mbar_wait(&p_ready[pb], (j >> 1) & 1, a.status)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {

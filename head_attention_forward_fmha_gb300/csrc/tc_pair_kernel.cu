@@ -329,9 +329,11 @@ __global__ void __launch_bounds__(PCfg<HD>::THREADS, 1)
                     }
                     tc_commit(&slot_empty[sk]);
                 }
+                // V_j's slot first: it has usually landed before P_j is written,
+                // and a barrier test costs this thread ~240 cycles
                 int sv = 0;
-                if (!(ok = mbar_wait(p_ready, j & 1, a.status))) break;
                 if (!(ok = slot_take(sv))) break;
+                if (!(ok = mbar_wait(p_ready, j & 1, a.status))) break;
                 ok = FMHA_IN_BOUNDS(sv >= 0 && sv < NSLOT, kSitePairVDesc, a.status);
                 if (!ok) break;
                 tc_fence_after();
