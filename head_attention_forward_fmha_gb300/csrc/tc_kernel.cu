@@ -14,7 +14,8 @@
 //               soon as QK_j has read it
 //   warp 6      TMA producer for V_j; a V stage is released after PV_j
 //   warp 1      TMEM owner and MMA issuer (one elected lane): QK runs two
-//               tiles ahead of PV (S is double-buffered), P is double-buffered
+//               tiles ahead of PV (three at hd <= 128 in the TS form, with a
+//               third S buffer), P is double-buffered
 //   warps 2..5  softmax: one query row per thread (its TMEM lane); reads S_j
 //               with tcgen05.ld, applies scale and mask, keeps the running max
 //               and sum (FA2 online softmax: commit e4ee9fd of the
@@ -57,17 +58,21 @@ struct TCfg {
     static constexpr int P_CHUNKS = (BN < 64 ? BN : 64) / 8;  // 16-byte chunks per row and group
     static constexpr int P_BYTES = TS ? 0 : BM * 128 * P_GROUPS;  // one P buffer (two are kept)
     static constexpr int THREADS = 224;
-    static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers (P over S in TS), then O
-    static constexpr int O_COL = 2 * BN;
+    // S buffers in TMEM (P over S in the TS form): three at hd <= 128 in the TS
+    // form, so that QK runs three tiles ahead of P V, two otherwise
+    static constexpr int NSB = (TS && HD <= 128) ? 3 : 2;
+    static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
+    static constexpr int O_COL = NSB * BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * KV_TILE;
     static constexpr int OFF_P = OFF_V + VST * KV_TILE;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1;
+    static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 3 * NSB + 1;
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
-    static_assert(O_COL + HD <= TMEM_COLS, "S double buffer + O must fit in TMEM");
+    static_assert(O_COL + HD <= TMEM_COLS, "S buffers + O must fit in TMEM");
+    static_assert(TS || NSB == 2, "the SS form's P buffers pair with two S buffers");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((KST + VST) * KV_TILE >= BM * HD * 4, "the epilogue stages fp32 O in the K/V stages");
 };
@@ -115,10 +120,11 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
     uint64_t* k_empty = k_full + KST;
     uint64_t* v_full = k_empty + KST;
     uint64_t* v_empty = v_full + VST;
-    uint64_t* s_full = v_empty + VST;  // [2] by S buffer
-    uint64_t* p_ready = s_full + 2;    // [2] by P buffer
-    uint64_t* o_done = p_ready + 2;    // [2] by P buffer: PV of a tile using that P buffer completed
-    uint64_t* mma_drain = o_done + 2;  // every MMA the issuer launched has completed (exit drain)
+    constexpr int NSB = C::NSB;
+    uint64_t* s_full = v_empty + VST;    // [NSB] by S buffer
+    uint64_t* p_ready = s_full + NSB;    // [NSB] by P buffer (the S buffer in the TS form)
+    uint64_t* o_done = p_ready + NSB;    // [NSB] by P buffer: PV of a tile using that P buffer completed
+    uint64_t* mma_drain = o_done + NSB;  // every MMA the issuer launched has completed (exit drain)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int b2 = 0; b2 < 2; ++b2) {
+        for (int b2 = 0; b2 < NSB; ++b2) {
             mbar_init(&s_full[b2], 1);
             mbar_init(&p_ready[b2], 128);
             mbar_init(&o_done[b2], 1);
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Order: QK_0, QK_1, then per tile j: PV_j, QK_{j+2}.
+        // Order: QK_0 .. QK_{NSB-1}, then per tile j: PV_j, QK_{j+NSB}.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, 1);
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
                 if (!FMHA_IN_BOUNDS(s >= 0 && s < KST, kSiteTcKDesc, a.status)) return false;
                 if (!mbar_wait(&k_full[s], (j / KST) & 1, a.status)) return false;
                 tc_fence_after();
-                const uint32_t d = tmem + C::S_COL0 + (j & 1) * BN;
+                const uint32_t d = tmem + C::S_COL0 + (j % NSB) * BN;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes into the swizzled row
@@ -279,29 +285,28 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
                     const uint64_t bd = smem_desc_sw128(k_addr + s * C::KV_TILE + (kk >> 2) * BN * 128 + off, 16, 1024);
                     tc_mma_f16(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(&s_full[j & 1]);
+                tc_commit(&s_full[j % NSB]);
                 tc_commit(&k_empty[s]);
                 return true;
             };
-            if (ok) ok = issue_qk(0);
-            if (ok && n_tiles > 1) ok = issue_qk(1);
+            for (int j = 0; ok && j < NSB && j < n_tiles; ++j) ok = issue_qk(j);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % VST;
-                const int pb = j & 1;
-                if (!FMHA_IN_BOUNDS(s >= 0 && s < VST && pb < 2, kSiteTcVDesc, a.status)) break;
+                const int pb = j % NSB;
+                if (!FMHA_IN_BOUNDS(s >= 0 && s < VST && pb < NSB, kSiteTcVDesc, a.status)) break;
                 // V_j has usually landed long before P_j: test it first, while the
                 // softmax still works, so that no barrier test (~240 cycles for
                 // this thread) stands between P_j and its MMAs
                 if (!mbar_wait(&v_full[s], (j / VST) & 1, a.status)) break;
-                if (!mbar_wait(&p_ready[pb], (j >> 1) & 1, a.status)) break;
+                if (!mbar_wait(&p_ready[pb], (j / NSB) & 1, a.status)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, BN * 128, 1024);
                     if constexpr (TS) {
-                        // A = P_j in TMEM: S buffer j & 1, 8 columns (16 bf16 keys) per MMA
-                        const uint32_t a_col = C::S_COL0 + (j & 1) * BN + kk * 8;
-                        if (!FMHA_IN_BOUNDS(a_col + 8 <= C::S_COL0 + 2 * BN, kSiteTcPTmem, a.status)) break;
+                        // A = P_j in TMEM: S buffer j % NSB, 8 columns (16 bf16 keys) per MMA
+                        const uint32_t a_col = C::S_COL0 + pb * BN + kk * 8;
+                        if (!FMHA_IN_BOUNDS(a_col + 8 <= C::S_COL0 + NSB * BN, kSiteTcPTmem, a.status)) break;
                         tc_mma_f16_ts(tmem + C::O_COL, tmem + a_col, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                     } else {
                         const uint64_t ad = smem_desc_sw128(
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
                 }
                 tc_commit(&o_done[pb]);
                 tc_commit(&v_empty[s]);
-                if (j + 2 < n_tiles && !issue_qk(j + 2)) break;
+                if (j + NSB < n_tiles && !issue_qk(j + NSB)) break;
             }
             // Exit drain: whatever the loop issued has completed before TMEM
             // and the operand buffers are released, even if a wait gave up.
@@ -334,15 +339,15 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
         float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int pb = j & 1;
-            if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status)) {
+            const int pb = j % NSB;
+            if (!mbar_wait(&s_full[pb], (j / NSB) & 1, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             float x[BN];
-            const uint32_t s_col = FMHA_IN_BOUNDS(C::S_COL0 + (j & 1) * BN + BN <= C::O_COL, kSiteTcSCol, a.status)
-                                       ? C::S_COL0 + (j & 1) * BN
+            const uint32_t s_col = FMHA_IN_BOUNDS(C::S_COL0 + pb * BN + BN <= C::O_COL, kSiteTcSCol, a.status)
+                                       ? C::S_COL0 + pb * BN
                                        : 0u;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
@@ -358,15 +363,15 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
             softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
             // SS: P buffer pb was last read by PV_{j-2}.  TS: P_j goes over S_j,
-            // whose QK the MMA issuer queued after PV_{j-2}, so S_j being ready
+            // whose QK the MMA issuer queued after PV_{j-NSB}, so S_j being ready
             // means that PV is done.  Either way a rescale of O needs PV_{j-1} done.
             if (rescale) {
-                if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status)) {
+                if (!mbar_wait(&o_done[(j - 1) % NSB], ((j - 1) / NSB) & 1, a.status)) {
                     ok = false;
                     break;
                 }
-            } else if (!TS && j >= 2) {
-                if (!mbar_wait(&o_done[pb], ((j >> 1) - 1) & 1, a.status)) {
+            } else if (!TS && j >= NSB) {
+                if (!mbar_wait(&o_done[pb], ((j / NSB) - 1) & 1, a.status)) {
                     ok = false;
                     break;
                 }
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
             mbar_arrive(&p_ready[pb]);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok && n_tiles > 0) ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
+        if (ok && n_tiles > 0) ok = mbar_wait(&o_done[(n_tiles - 1) % NSB], ((n_tiles - 1) / NSB) & 1, a.status);
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
