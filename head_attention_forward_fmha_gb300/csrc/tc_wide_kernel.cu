@@ -7,9 +7,10 @@
 //   S_j  = sum_c Q[:, c] K_j[:, c]^T   over the 8 64-column chunks c of hd
 //          (every block computes the full S; it is cheap next to the loads)
 //   O_h += P_j V_j[:, 256h : 256h + 256]
-// Q and K stream through one ring of 16 KB slots chunk by chunk (Q chunks
-// come from L2 after the first block reads them), then the four 64-column V
-// chunks of this half.  TMEM: two S buffers (2 x 128 columns) + O half (256).
+// Q and K stream through one ring chunk by chunk, Q chunk c and K chunk c in
+// one 32 KB item (Q chunks come from L2 after the first block reads them),
+// then the four 64-column V chunks of this half in two items.  TMEM: two S
+// buffers (2 x 128 columns) + O half (256).
 // Softmax, lazy rescale and the epilogue are those of tc_kernel.cu; both
 // halves compute identical (max, sum), and half 0 writes the LSE.
 #include <algorithm>
