@@ -18,7 +18,10 @@ namespace fmha {
 // exceeds it by more than 8 (log2 units); then alpha = 2^(m_old - m_new) and
 // the caller rescales O.  Probabilities are therefore <= 2^8.  The
 // scale-and-subtract and both sums run on packed fp32 pairs.
-template <int BN>
+// With LO = false the rounded sum is left to the caller (l_o is not touched):
+// the row-tile kernel at hd 64 gets it from the tensor core, as one more column
+// of O against a column of ones.
+template <int BN, bool LO = true>
 __device__ __forceinline__ void softmax_row_tile(float (&x)[BN], uint32_t (&p)[BN / 2], int key0, int jlo, int jhi,
                                                  float sl2, float& m_ref, float& l, float& l_o, float& alpha) {
     const bool full = key0 >= jlo && key0 + BN - 1 <= jhi;
@@ -69,15 +72,18 @@ __device__ __forceinline__ void softmax_row_tile(float (&x)[BN], uint32_t (&p)[B
         const uint32_t pk = pack_bf16x2(y0, y1);
         p[i] = pk;
         s2[i & 1] = add_f32x2(s2[i & 1], f32x2(y0, y1));
-        r2[i & 1] = add_f32x2(r2[i & 1], f32x2(bf16_lo(pk), bf16_hi(pk)));
+        if constexpr (LO) r2[i & 1] = add_f32x2(r2[i & 1], f32x2(bf16_lo(pk), bf16_hi(pk)));
     }
-    float a0, a1, b0, b1, c0, c1, d0, d1;
+    float a0, a1, b0, b1;
     f32x2_split(s2[0], a0, a1);
     f32x2_split(s2[1], b0, b1);
-    f32x2_split(r2[0], c0, c1);
-    f32x2_split(r2[1], d0, d1);
     l = l * alpha + ((a0 + a1) + (b0 + b1));
-    l_o = l_o * alpha + ((c0 + c1) + (d0 + d1));
+    if constexpr (LO) {
+        float c0, c1, d0, d1;
+        f32x2_split(r2[0], c0, c1);
+        f32x2_split(r2[1], d0, d1);
+        l_o = l_o * alpha + ((c0 + c1) + (d0 + d1));
+    }
     m_ref = m_new;
 }
 

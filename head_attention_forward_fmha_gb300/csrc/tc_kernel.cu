@@ -63,15 +63,22 @@ struct TCfg {
     static constexpr int NSB = (TS && HD <= 128) ? 3 : 2;
     static constexpr int S_COL0 = 0;                   // TMEM columns: S buffers, then O
     static constexpr int O_COL = NSB * BN;
+    // TS at hd 64: P V runs with N = hd + 16, the extra columns of B a tile of
+    // ones in shared memory, so O's column hd accumulates the sum of the
+    // bf16-rounded P (the divisor of O) and the softmax does not
+    static constexpr bool ONES = TS && HD == 64;
+    static constexpr int O_N = HD + (ONES ? 16 : 0);  // O columns written by P V
+    static constexpr int ONES_BYTES = ONES ? BN * 128 : 0;
     static constexpr int TMEM_COLS = 512;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * KV_TILE;
     static constexpr int OFF_P = OFF_V + VST * KV_TILE;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_ONES = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
     static constexpr int N_BARS = 1 + 2 * KST + 2 * VST + 3 * NSB + 1;
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
-    static_assert(O_COL + HD <= TMEM_COLS, "S buffers + O must fit in TMEM");
+    static_assert(O_COL + (O_N + 31) / 32 * 32 <= TMEM_COLS, "S buffers + O must fit in TMEM");
     static_assert(TS || NSB == 2, "the SS form's P buffers pair with two S buffers");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((KST + VST) * KV_TILE >= BM * HD * 4, "the epilogue stages fp32 O in the K/V stages");
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
     uint8_t* sk = smem + C::OFF_K;
     uint8_t* sv = smem + C::OFF_V;
     uint8_t* sp = smem + C::OFF_P;
+    uint8_t* sones = smem + C::OFF_ONES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
@@ -221,6 +229,12 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    if constexpr (C::ONES) {
+        // bf16 1.0 in every element: which columns the swizzle puts where does not matter
+        for (int i = threadIdx.x; i < C::ONES_BYTES / 16; i += C::THREADS)
+            reinterpret_cast<uint4*>(sones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -268,7 +282,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
         // Order: QK_0 .. QK_{NSB-1}, then per tile j: PV_j, QK_{j+NSB}.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, 1);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, C::O_N, 1);
             const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk), v_addr = smem_u32(sv),
                            p_addr = smem_u32(sp);
             bool ok = mbar_wait(q_full, 0, a.status);
@@ -302,7 +316,10 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, BN * 128, 1024);
+                    // V's 64-column boxes one tile apart, or at hd 64 the tile of ones
+                    // as the second box (the leading byte offset spans the gap)
+                    const uint32_t lbo = C::ONES ? smem_u32(sones) - (v_addr + s * C::KV_TILE) : BN * 128;
+                    const uint64_t bd = smem_desc_sw128(v_addr + s * C::KV_TILE + kk * 16 * 128, lbo, 1024);
                     if constexpr (TS) {
                         // A = P_j in TMEM: S buffer j % NSB, 8 columns (16 bf16 keys) per MMA
                         const uint32_t a_col = C::S_COL0 + pb * BN + kk * 8;
@@ -360,7 +377,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
             // Exponentials and the row sum before waiting on the tensor core.
             float alpha;
             uint32_t pk[BN / 2];
-            softmax_row_tile<BN>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
+            softmax_row_tile<BN, !C::ONES>(x, pk, k_lo + j * BN, jlo, jhi, a.scale_log2, m_ref, l, l_o, alpha);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
             // SS: P buffer pb was last read by PV_{j-2}.  TS: P_j goes over S_j,
             // whose QK the MMA issuer queued after PV_{j-NSB}, so S_j being ready
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
             if (rescale) {
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = 0; c < (C::O_N + 31) / 32; ++c) {  // with the column of rounded sums
                     float ov[32];
                     tmem_ld32(t_lane + C::O_COL + c * 32, ov);
                     tmem_wait_ld();
@@ -406,6 +423,13 @@ __global__ void __launch_bounds__(TCfg<HD, TS>::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) atomicOr(abort_flag, 1);
         tc_fence_after();
+        if constexpr (C::ONES) {  // the sum of the rounded P, from O's column hd (warp-collective load)
+            l_o = 0.f;
+            if (ok && n_tiles > 0) {
+                l_o = tmem_ld1(t_lane + C::O_COL + HD);
+                tmem_wait_ld();
+            }
+        }
         float inv, lse;
         // query head of this row: kvh * G + (row within the slab) / T
         finish_row(m_ref, l, l_o,
