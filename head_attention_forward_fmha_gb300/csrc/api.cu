@@ -370,7 +370,7 @@ enum RowsType { kRowsBf16, kRowsF32, kRowsF16 };
 // A row-tile tensor [slabs, R, hd] (Q, O, or partials) viewed as 3-D;
 // boxes of 128 bytes of columns x kTcRows rows, 128-byte swizzle.
 int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long slabs, RowsType type,
-                  const char* what) {
+                  const char* what, int box_rows = kTcRows) {
     if (!tensor_map_encoder()) return fail(FMHA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
     const int esz = type == kRowsF32 ? 4 : 2;
     const CUtensorMapDataType dt = type == kRowsF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -378,7 +378,7 @@ int make_rows_map(CUtensorMap* m, const void* base, int hd, int R, long long sla
                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)R, (cuuint64_t)slabs};
     cuuint64_t strides[2] = {(cuuint64_t)hd * esz, (cuuint64_t)R * hd * esz};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kTcRows, 1};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
     CUresult r = g_encode(m, dt, 3,
                           const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -424,7 +424,8 @@ int run_kernel(const void* q, const void* k, const void* v, const Problem& p, co
         L.p = p;
         L.sp = sp;
         L.status = status;
-        int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, kRowsBf16, "Q");
+        int rc = make_rows_map(&L.tmap_q, q, p.hd, p.R, slabs, kRowsBf16, "Q",
+                               path == Path::TensorCoreWide ? tc_wide_q_box_rows(p, sp) : kTcRows);
         if (rc) return rc;
         // An NVFP4 output is stored row by row without a tensor map; the O map
         // is then built over Q (same shape and type) and never stored through.

@@ -80,6 +80,10 @@ cudaError_t launch_tc(const TcLaunch& L, cudaStream_t stream);
 // hd = 512 variant (tc_wide_kernel.cu): two thread blocks per row tile, one
 // per half of the head dim of O.
 int tc_wide_kv_tile();
+// Rows of the Q map's TMA box for the hd-512 kernel: 32 or 64 where its blocks
+// keep a compact resident Q (at most that many query rows per KV head), else
+// kTcRows.
+int tc_wide_q_box_rows(const Problem& p, const SplitPlan& sp);
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream);
 // Two 128-row tiles per thread block (tc_pair_kernel.cu), hd 64 and 128: for
 // KV heads with more than 128 query rows; the same Q, O, K and V maps as

@@ -30,10 +30,14 @@ namespace {
 // 32 KB items (a block with a single KV tile reads Q once either way).
 // QRES = true (blocks with two or more KV tiles): the 128 KB Q tile is loaded
 // once and stays resident, and only K and V chunks stream, through three
-// 32 KB items; the epilogue then stages O in the Q region.  In both, P goes
-// over S in tensor memory and the P V MMAs read it from there (the TS form),
-// so no shared memory holds P.
-template <bool QRES>
+// 32 KB items; the epilogue then stages O in the Q region and the drained ring.
+// With at most 32 (64) query rows per KV head, QROWS = 32 (64): only those
+// rows of each Q chunk are loaded, the chunks 4 KB (8 KB) apart.  The MMA
+// still reads 128 rows of A per chunk, the rows past QROWS falling on the next
+// chunks (or a zeroed tail); their S rows belong to no query and are masked.
+// Q then takes 44 KB (72 KB) and the ring five (four) items.  In all, P goes over S in tensor memory and the P V MMAs
+// read it from there (the TS form), so no shared memory holds P.
+template <bool QRES, int QROWS = 128>
 struct WCfgT {
     static constexpr int HD = 512;
     static constexpr int HALF = 256;
@@ -43,7 +47,11 @@ struct WCfgT {
     static constexpr int Q_CHUNKS = HD / 64;
     static constexpr int CPI = 2;                      // chunks per ring item
     static constexpr int ITEM_BYTES = CPI * SLOT_BYTES;
-    static constexpr int NSLOT = QRES ? 3 : 4;         // ring items
+    static constexpr int Q_ROWS = QRES ? QROWS : 128;  // rows of each Q chunk loaded
+    static constexpr int Q_STRIDE = Q_ROWS * 128;      // bytes between resident Q chunks
+    // the last chunk's MMA reads a whole 128-row operand
+    static constexpr int Q_REGION = QRES ? (Q_CHUNKS - 1) * Q_STRIDE + SLOT_BYTES : 0;
+    static constexpr int NSLOT = QRES ? (Q_ROWS == 128 ? 3 : Q_ROWS == 64 ? 4 : 5) : 4;  // ring items
     static constexpr int QK_ITEMS = QRES ? Q_CHUNKS / CPI : Q_CHUNKS;  // (K, K) or (Q, K) chunk pairs per tile
     static constexpr int V_CHUNKS = HALF / 64;
     static constexpr int V_ITEMS = V_CHUNKS / CPI;
@@ -61,16 +69,18 @@ struct WCfgT {
     static constexpr int THREADS = 192;
     static constexpr int O_COL = 2 * BN;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int OFF_Q = 0;                                   // QRES: resident Q (128 KB)
-    static constexpr int OFF_RING = QRES ? Q_CHUNKS * SLOT_BYTES : 0;
+    static constexpr int OFF_Q = 0;                                   // QRES: resident Q
+    static constexpr int OFF_RING = OFF_Q + Q_REGION;
     static constexpr int OFF_P = OFF_RING + NSLOT * ITEM_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging (128 KB)
+    static constexpr int OFF_STAGE = QRES ? OFF_Q : OFF_RING;         // epilogue staging
+    static constexpr int STAGE_BYTES = OFF_P - OFF_STAGE;
     static constexpr int N_BARS = 2 * NSLOT + 2 + 2 + 2 + 1 + (QRES ? 1 : 0);
     static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
     static_assert(O_COL + HALF <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((QRES ? Q_CHUNKS * SLOT_BYTES : NSLOT * ITEM_BYTES) >= BM * HALF * 4, "the epilogue stages fp32 O");
+    static_assert(STAGE_BYTES >= BM * HALF * 4, "the epilogue stages fp32 O");
+    static_assert(Q_ROWS == 128 || Q_ROWS == 64 || Q_ROWS == 32, "resident Q rows");
 };
 using WCfg = WCfgT<false>;
 
@@ -98,12 +108,12 @@ __device__ __forceinline__ void w_attended(int t, const WideArgs& a, int& lo, in
     if (a.window > 0) lo = max(lo, p - a.window + 1);
 }
 
-template <int EPI, bool QRES>
+template <int EPI, bool QRES, int QROWS>
 __global__ void __launch_bounds__(WCfg::THREADS, 1)
     fwd_tc_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                        const WideArgs a) {
-    using C = WCfgT<QRES>;
+    using C = WCfgT<QRES, QROWS>;
     constexpr int BM = C::BM, BN = C::BN;
     constexpr bool SINK = EPI == kEpiSink;
     launch_dependents();  // the merge grid may be scheduled now; it waits for this grid's results
@@ -230,15 +240,24 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             pol_q = l2_policy_evict_last();
             grid_dependency_wait();  // the preceding kernel's writes (Q, K, V) are visible
             if (QRES && FMHA_IN_BOUNDS(r_begin >= 0 && r_begin < a.R && slab < (int)gridDim.z, kSiteWideQ, a.status)) {
-                mbar_arrive_expect_tx(q_full, C::Q_CHUNKS * C::SLOT_BYTES);
+                mbar_arrive_expect_tx(q_full, C::Q_CHUNKS * C::Q_STRIDE);
                 for (int c = 0; c < C::Q_CHUNKS; ++c)
-                    tma_load_3d_hint(qres + c * C::SLOT_BYTES, &tmq, c * 64, r_begin, slab, q_full, pol_q);
+                    tma_load_3d_hint(qres + c * C::Q_STRIDE, &tmq, c * 64, r_begin, slab, q_full, pol_q);
                 q_issued = true;
             }
             for (int i = 0; i < min(C::NSLOT, n_items); ++i) {
                 if (!issue_item(i)) break;
                 ++issued;
             }
+        }
+    }
+    if constexpr (C::Q_ROWS < 128) {
+        // the last chunks' A operands run past the loaded Q rows into this tail
+        if (warp >= 2) {
+            constexpr int TAIL = C::Q_REGION - C::Q_CHUNKS * C::Q_STRIDE;
+            uint4* tail = reinterpret_cast<uint4*>(qres + C::Q_CHUNKS * C::Q_STRIDE);
+            for (int i = threadIdx.x - 64; i < TAIL / 16; i += 128) tail[i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
         }
     }
     if (warp == 1) {
@@ -291,7 +310,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                     for (int sub = 0; sub < (QRES ? 2 : 1); ++sub) {
                         const int ch = QRES ? 2 * c + sub : c;  // 64-column chunk of hd
                         // A: Q chunk ch (resident, or the item's first half); B: its K chunk
-                        const uint32_t a_base = QRES ? q_addr + ch * C::SLOT_BYTES : item_addr;
+                        const uint32_t a_base = QRES ? q_addr + ch * C::Q_STRIDE : item_addr;
                         const uint32_t b_base = QRES ? item_addr + sub * C::SLOT_BYTES : item_addr + C::SLOT_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -444,7 +463,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         }
         // This half of O -> shared memory (the drained ring) -> TMA store.
         const int pslab = split * (int)(a.rows_total / a.R) + slab;
-        constexpr int kStageBytes = QRES ? C::Q_CHUNKS * C::SLOT_BYTES : C::NSLOT * C::ITEM_BYTES;
+        constexpr int kStageBytes = C::STAGE_BYTES;
         const int3 ext = make_int3(C::HD, a.R, (int)(a.to_partials ? gridDim.y * gridDim.z : gridDim.z));
         if constexpr (EPI == kEpiNvfp4) {
             // quantised in registers and stored per row; rows past the slab's
@@ -494,15 +513,23 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
 
 int tc_wide_kv_tile() { return WCfg::BN; }
 
-template <int EPI, bool QRES>
+// Q stays resident when a block may see two or more 128-key tiles, and then
+// only 32 or 64 rows of each chunk are loaded if no KV head has more query rows.
+int tc_wide_q_box_rows(const Problem& p, const SplitPlan& sp) {
+    const int span = std::min(sp.kv_chunk, p.s_k);
+    if (span <= WCfg::BN) return 128;
+    return p.R <= 32 ? 32 : p.R <= 64 ? 64 : 128;
+}
+
+template <int EPI, bool QRES, int QROWS>
 cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
-    using C = WCfgT<QRES>;
+    using C = WCfgT<QRES, QROWS>;
     static std::atomic<bool> attr_set[128];  // set once per device; any host thread may set it
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<EPI, QRES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fwd_tc_wide_kernel<EPI, QRES, QROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 128) attr_set[dev] = true;
@@ -537,14 +564,16 @@ cudaError_t launch_wide_t(const TcLaunch& L, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {programmatic_launch_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<EPI, QRES>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
+    return cudaLaunchKernelEx(&cfg, fwd_tc_wide_kernel<EPI, QRES, QROWS>, L.tmap_q, L.tmap_k, L.tmap_v, L.tmap_o, a);
 }
 
 template <int EPI>
 cudaError_t launch_wide_q(const TcLaunch& L, cudaStream_t stream) {
-    // Q stays resident when a block may see two or more 128-key tiles.
+    const int rows = tc_wide_q_box_rows(L.p, L.sp);
+    if (rows == 32) return launch_wide_t<EPI, true, 32>(L, stream);
+    if (rows == 64) return launch_wide_t<EPI, true, 64>(L, stream);
     const int span = std::min(L.sp.kv_chunk, L.p.s_k);
-    return span > WCfg::BN ? launch_wide_t<EPI, true>(L, stream) : launch_wide_t<EPI, false>(L, stream);
+    return span > WCfg::BN ? launch_wide_t<EPI, true, 128>(L, stream) : launch_wide_t<EPI, false, 128>(L, stream);
 }
 
 cudaError_t launch_tc_wide(const TcLaunch& L, cudaStream_t stream) {

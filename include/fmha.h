@@ -156,8 +156,9 @@ int fmha_merge(const float* o_parts, const float* lse_parts, int n_splits,
  *   FMHA_PARTS_F16: o_parts fp16 [n_splits, batch, n_h, T, hd] holding
  *     O_i * 2^-k, and range_parts fp32 [n_splits, batch, n_h, T, 2] holding
  *     2^k for each 256-column half of each row; k is chosen per half row so
- *     that its largest |O_i| lies in [2^14, 2^15), so every finite partial
- *     keeps fp16's 11 significant bits and none overflows.  Half the bytes of
+ *     that its largest |O_i| * 2^-k lies in [2^14, 2^15) before rounding (so
+ *     in [2^14, 2^15] stored), so every finite partial keeps fp16's 11
+ *     significant bits and none overflows.  Half the bytes of
  *     FMHA_PARTS_F32 (for callers that move partials elsewhere before merging;
  *     fmha_fwd uses this format internally at hd 512).  Written only by the
  *     hd-512 tensor-core kernel: hd = 512 and fmha_fwd_plan reporting kernel 3,

@@ -40,6 +40,14 @@ SHAPES = [
     W("k17_T128_causal_hd512", 1, 2, 2, 128, 260, 512, causal=True),
     W("k18_hd512_G64_T2_window", 1, 64, 1, 2, 700, 512, window=300),
     W("k19_hd512_R200", 1, 200, 1, 1, 129, 512),
+    # hd 512, at most 32 or 64 query rows per KV head and blocks of two or
+    # more KV tiles: the compact resident Q (32 or 64 rows per chunk)
+    W("k20_hd512_T32_causal_q32", 1, 2, 2, 32, 600, 512, causal=True),
+    W("k21_hd512_G4_T8_window_q32", 1, 8, 2, 8, 1000, 512, window=700),
+    W("k22_hd512_T17_causal_q32", 1, 2, 2, 17, 300, 512, causal=True),
+    W("k23_hd512_T1_q32", 2, 4, 4, 1, 700, 512),
+    W("k24_hd512_T64_causal_q64", 1, 2, 2, 64, 600, 512, causal=True),
+    W("k25_hd512_G3_T15_window_q64", 1, 6, 2, 15, 900, 512, window=500),
 ]
 
 
@@ -167,3 +175,51 @@ def test_f16_partial_format_matches_oracle_and_fmha_fwd(chunk):
     torch.cuda.synchronize()
     assert op2.shape[0] == n_plan
     assert torch.equal(o2, o3) and torch.equal(lse2, lse3)
+    _check_f16_ranges(op, "chunk %d" % chunk)
+    _check_f16_ranges(op2, "plan chunk")
+
+
+def _check_f16_ranges(op, label):
+    """The range factor of each (split, row, half): the half row's largest stored
+    |O_i 2^-k| lies in [2^14, 2^15) before rounding, so in [2^14, 2^15] in fp16 (whose
+    spacing there is 16), unless the half row is all zero."""
+    n, b, n_h, T, hd = op.shape
+    mh = op.float().abs().reshape(n, b, n_h, T, 2, hd // 2).amax(-1)
+    assert bool((mh <= 2.0 ** 15).all()), label + ": a stored fp16 partial exceeds 2^15"
+    nz = mh > 0
+    assert bool((mh[nz] >= 2.0 ** 14).all()), "%s: smallest half-row maximum %.3e < 2^14" % (label, mh[nz].min().item())
+
+
+@pytest.mark.parametrize("chunk", [128, 0])
+def test_f16_partials_beside_a_large_v_row_of_negligible_weight(chunk):
+    """One key's V row is 2^60 times the rest while its K row is zero and Q is
+    scaled by 30, so every row gives that key a weight below e^-40: |V| over the
+    tile is no bound worth scaling the fp16 partials by (the other values would
+    flush to zero), and the range factors must follow |O| itself.  chunk 0 = the
+    plan's."""
+    w = W("hd512_v_outlier", 2, 128, 1, 1, 700, 512, window=500)
+    q, k, v = inputs.make_inputs(w, seed=15)
+    q = (q.double() * 30).to(torch.bfloat16)
+    key = 330
+    k[:, :, key, :] = 0
+    v[:, :, key, :] = (v[:, :, key, :].double() * 2.0 ** 60).to(torch.bfloat16)
+    if chunk == 0:
+        _, chunk = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, w.window, w.causal)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    op, lp, rp = binding.fmha_fwd_splitkv_f16(qd, kd, vd, chunk, scale=w.scale, window=w.window)
+    o, lse = binding.fmha_merge_f16(op, lp, rp)
+    o3, lse3 = binding.fmha_fwd(qd, kd, vd, scale=w.scale, window=w.window)
+    torch.cuda.synchronize()
+    binding.fmha_check_device_status()
+    n, b, n_h, T, hd = op.shape
+    deq = op.double() * rp.double().repeat_interleave(hd // 2, dim=-1)
+    qb, kb, vb = to_np_bits(q), to_np_bits(k), to_np_bits(v)
+    op_ref, lp_ref = oracle.partials(qb, kb, vb, w.scale, chunk, w.window, False)
+    label = "V outlier, chunk %d" % chunk
+    compare(deq, lp, op_ref, lp_ref, label + " partials")
+    o_ref, lse_ref = oracle.merge(op_ref, lp_ref)
+    compare(o, lse, o_ref, lse_ref, label + " merged")
+    cosine_per_head(o, o_ref, label)
+    o_full, lse_full = oracle.attention(qb, kb, vb, w.scale, w.window, w.causal)
+    compare(o3, lse3, o_full, lse_full, label + " fmha_fwd")
+    _check_f16_ranges(op, label)

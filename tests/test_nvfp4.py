@@ -70,6 +70,7 @@ SHAPES = [
     # hd-512 tensor-core kernel, unsplit and split (merge of fp16 partials)
     W("wide_hd512_T128", 1, 2, 2, 128, 130, 512),
     W("wide_split_mqa", 2, 128, 1, 1, 512, 512),
+    W("wide_hd512_T32_q32", 4, 16, 16, 32, 512, 512, causal=True),
     # no key at all: O = 0 -> zero scales and codes, LSE = -inf
     W("no_key", 1, 2, 1, 2, 0, 64),
 ]

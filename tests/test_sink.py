@@ -27,6 +27,7 @@ SHAPES = [
     W("sink_prefill_hd256", 2, 4, 4, 128, 256, 256, causal=True),
     W("sink_mqa_hd512_split", 2, 128, 1, 1, 512, 512),
     W("sink_hd512_R200", 1, 200, 1, 1, 129, 512),
+    W("sink_hd512_T32_q32", 4, 16, 16, 32, 512, 512, causal=True),
 ]
 
 
