@@ -327,8 +327,10 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
             ok = issue_qk(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
-                if (!(ok = mbar_wait(&p_ready[j & 1], (j >> 1) & 1, a.status))) break;
-                tc_fence_after();
+                // One-tile blocks test V_j first: it lands while the softmax still
+                // works on S_j, so only the P_j test remains once P_j is written
+                // (with a resident Q the other order measured faster).
+                if (QRES && !(ok = mbar_wait(&p_ready[j & 1], (j >> 1) & 1, a.status))) break;
                 int sv[C::V_ITEMS];
                 for (int c = 0; c < C::V_ITEMS && ok; ++c) {
                     ok = slot_take(sv[c]);
@@ -337,6 +339,7 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
                                             kSiteWideVSlots, a.status);
                 }
                 if (!ok) break;
+                if (!QRES && !(ok = mbar_wait(&p_ready[j & 1], (j >> 1) & 1, a.status))) break;
                 tc_fence_after();
                 // A: P_j in TMEM over S_j (8 columns = 16 keys per MMA); B: each
                 // group of V_GROUP 64-column V boxes, one chunk apart (the
