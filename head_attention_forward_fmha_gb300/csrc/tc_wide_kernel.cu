@@ -26,8 +26,10 @@ namespace {
 // Every ring item holds two 64-column chunks under one barrier: a barrier
 // test costs the MMA-issuing thread ~240 cycles after N = 128 MMAs, so fewer
 // and larger items keep the tensor pipe fed.  QRES = false: the items are
-// (Q chunk c, K chunk c) pairs, then the V chunks, through a ring of four
-// 32 KB items (a block with a single KV tile reads Q once either way).
+// (Q chunk c, K chunk c) pairs, then the V chunks, through a ring of six
+// 32 KB items (a block with a single KV tile reads Q once either way; a
+// seventh item would leave no shared memory for the merge's blocks, which
+// then could not become resident before this grid ends).
 // QRES = true (blocks with two or more KV tiles): the 128 KB Q tile is loaded
 // once and stays resident, and only K and V chunks stream, through three
 // 32 KB items; the epilogue then stages O in the Q region and the drained ring.
@@ -35,8 +37,9 @@ namespace {
 // rows of each Q chunk are loaded, the chunks 4 KB (8 KB) apart.  The MMA
 // still reads 128 rows of A per chunk, the rows past QROWS falling on the next
 // chunks (or a zeroed tail); their S rows belong to no query and are masked.
-// Q then takes 44 KB (72 KB) and the ring five (four) items.  In all, P goes over S in tensor memory and the P V MMAs
-// read it from there (the TS form), so no shared memory holds P.
+// Q then takes 44 KB (72 KB) and the ring five (four) items.  In all, P goes
+// over S in tensor memory and the P V MMAs read it from there (the TS form),
+// so no shared memory holds P.
 template <bool QRES, int QROWS = 128>
 struct WCfgT {
     static constexpr int HD = 512;
@@ -51,19 +54,19 @@ struct WCfgT {
     static constexpr int Q_STRIDE = Q_ROWS * 128;      // bytes between resident Q chunks
     // the last chunk's MMA reads a whole 128-row operand
     static constexpr int Q_REGION = QRES ? (Q_CHUNKS - 1) * Q_STRIDE + SLOT_BYTES : 0;
-    static constexpr int NSLOT = QRES ? (Q_ROWS == 128 ? 3 : Q_ROWS == 64 ? 4 : 5) : 4;  // ring items
+    static constexpr int NSLOT = QRES ? (Q_ROWS == 128 ? 3 : Q_ROWS == 64 ? 4 : 5) : 6;  // ring items
     static constexpr int QK_ITEMS = QRES ? Q_CHUNKS / CPI : Q_CHUNKS;  // (K, K) or (Q, K) chunk pairs per tile
     static constexpr int V_CHUNKS = HALF / 64;
     static constexpr int V_ITEMS = V_CHUNKS / CPI;
     static constexpr int TILE_ITEMS = QK_ITEMS + V_ITEMS;
     // P V is one MMA of N = 64 V_GROUP per group of V_GROUP chunks and 16 keys,
     // the group's chunks one SLOT_BYTES apart: one N = 256 MMA over the two V
-    // items of the 4-item ring (a tile's V items start at an even index, so
-    // they never wrap around the ring); two N = 128 MMAs, one per item, with
-    // the resident Q.
+    // items of a one-tile block (items QK_ITEMS and QK_ITEMS + 1, in
+    // consecutive slots of the ring; such a block never holds a second tile);
+    // two N = 128 MMAs, one per item, with the resident Q.
     static constexpr int V_GROUP = QRES ? 2 : 4;
     static constexpr int V_GROUP_ITEMS = V_GROUP / CPI;
-    static_assert(QK_ITEMS % V_GROUP_ITEMS == 0 && NSLOT % V_GROUP_ITEMS == 0 && V_ITEMS % V_GROUP_ITEMS == 0,
+    static_assert(QRES ? V_GROUP_ITEMS == 1 : (QK_ITEMS % NSLOT + V_ITEMS <= NSLOT && V_GROUP_ITEMS == V_ITEMS),
                   "V slot groups must be contiguous");
     static constexpr int P_BYTES = 0;  // P lives in tensor memory
     static constexpr int THREADS = 192;
@@ -160,7 +163,11 @@ __global__ void __launch_bounds__(WCfg::THREADS, 1)
         u_hi = h1;
     }
     const int k_lo = max(c_lo, u_lo), k_hi = min(c_hi, u_hi + 1);
-    const int n_tiles = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
+    const int n_tiles_all = (k_hi > k_lo) ? (k_hi - k_lo + BN - 1) / BN : 0;
+    // without a resident Q a block holds one tile (the host picks the resident
+    // Q for longer spans), which its ring item order relies on
+    const int n_tiles =
+        (QRES || FMHA_IN_BOUNDS(n_tiles_all <= 1, kSiteWideTiles, a.status)) ? n_tiles_all : 0;
 
     // Producer item sequence: QK(0), then for each tile j: QK(j+1) (if any)
     // and V(j) -- the order the MMA warp consumes them in.  Item i -> kind
