@@ -65,7 +65,6 @@ enum CheckSite : unsigned {
     kSiteWideLse = 0x207,
     kSiteWideRange = 0x208,  // range factor index of an fp16 partial
     kSiteWideFp4 = 0x209,    // NVFP4 output row
-    kSiteWideTiles = 0x20a,  // a block without a resident Q holds at most one KV tile
     kSiteDecQRow = 0x301,    // Q row loaded from global memory
     kSiteDecQSmem = 0x302,   // Q staging offset
     kSiteDecKVLoad = 0x303,  // K/V stage: first key, stage offset

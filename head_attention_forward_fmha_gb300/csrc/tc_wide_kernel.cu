@@ -23,6 +23,10 @@
 namespace fmha {
 namespace {
 
+// Index-check site of this kernel beside those in ptx.cuh: a block without a
+// resident Q holds at most one KV tile.
+constexpr unsigned kSiteWideTiles = 0x20a;
+
 // Every ring item holds two 64-column chunks under one barrier: a barrier
 // test costs the MMA-issuing thread ~240 cycles after N = 128 MMAs, so fewer
 // and larger items keep the tensor pipe fed.  QRES = false: the items are
