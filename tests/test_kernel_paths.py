@@ -223,3 +223,57 @@ def test_f16_partials_beside_a_large_v_row_of_negligible_weight(chunk):
     o_full, lse_full = oracle.attention(qb, kb, vb, w.scale, w.window, w.causal)
     compare(o3, lse3, o_full, lse_full, label + " fmha_fwd")
     _check_f16_ranges(op, label)
+
+
+BACK_TO_BACK_SHAPES = [
+    W("cnt_mqa", 2, 128, 1, 1, 512, 512),
+    W("cnt_R200_two_row_tiles", 1, 200, 1, 1, 600, 512),
+    W("cnt_T32_q32", 1, 4, 4, 32, 700, 512),
+    W("cnt_G32_R32", 3, 64, 2, 1, 900, 512),
+    W("cnt_mqa_8_chunks", 2, 128, 1, 1, 2000, 512),
+]
+
+
+def test_hd512_split_calls_back_to_back_and_graph_replays():
+    """fmha_fwd at hd 512 with split KV (fp16 partials in the stream's workspace,
+    then the merge as a programmatic dependent): calls of different shapes back
+    to back on one stream, so that each reuses the workspace and its merge
+    overlaps the next call's split kernel set-up, then one shape captured in a
+    CUDA graph and replayed with fresh inputs, must each match the oracle."""
+    stream = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(stream):
+        for rep in range(2):
+            for i, w in enumerate(BACK_TO_BACK_SHAPES):
+                n, _, kern = binding.fmha_fwd_plan(w.batch, w.n_h, w.n_kv_h, w.T, w.s_k, w.hd, with_kernel=True)
+                assert n > 1 and kern == "fwd_tc_wide", (w.name, n, kern)
+                (q, k, v), (qd, kd, vd) = device_inputs(w, seed=40 + 7 * rep + i)
+                o, lse = binding.fmha_fwd(qd, kd, vd, scale=w.scale, stream=stream)
+                outs.append((w, q, k, v, o, lse))
+    stream.synchronize()
+    binding.fmha_check_device_status()
+    for w, q, k, v, o, lse in outs:
+        o_ref, lse_ref = oracle_full(w, q, k, v)
+        compare(o, lse, o_ref, lse_ref, w.name)
+        cosine_per_head(o, o_ref, w.name)
+
+    w = BACK_TO_BACK_SHAPES[0]
+    (q, k, v), (qd, kd, vd) = device_inputs(w, seed=60)
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=qd.device)
+    with torch.cuda.stream(stream):
+        binding.fmha_fwd(qd, kd, vd, o, lse, scale=w.scale, stream=stream)  # workspaces exist before capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        binding.fmha_fwd(qd, kd, vd, o, lse, scale=w.scale, stream=stream)
+    for rep in range(3):
+        (q, k, v), _ = device_inputs(w, seed=61 + rep)
+        qd.copy_(q.cuda())
+        kd.copy_(k.cuda())
+        vd.copy_(v.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        binding.fmha_check_device_status()
+        o_ref, lse_ref = oracle_full(w, q, k, v)
+        compare(o, lse, o_ref, lse_ref, "graph replay %d" % rep)
